@@ -1,0 +1,361 @@
+"""Checks that pin the oracle to facts other than itself.
+
+Each pin is a function that raises AssertionError when the oracle disagrees
+with the pages' worked examples, a closed form, an invariant, or a library
+routine.  tests/test_oracle_pins.py runs them against the oracle;
+tests/test_oracle_mutations.py runs them against copies of the oracle with a
+planted mistake and requires each mistake to be caught.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def golden(name: str) -> dict:
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _rand16(shape, dtype, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(*shape, generator=g).to(dtype)
+
+
+def _pool(NB, Hkv, B, d, dtype, seed):
+    return oracle.bits16(_rand16((NB, Hkv, B, d), dtype, seed))
+
+
+# -- decoding of the 16-bit formats ---------------------------------------------
+
+def pin_decode_f16_all_patterns():
+    """Every binary16 pattern decodes as numpy's float16 -> float64."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    got = oracle.decode16(bits, "f16")
+    want = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+
+
+def pin_decode_bf16_all_patterns():
+    """Every bfloat16 pattern decodes as torch's bfloat16 -> float64."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    want = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+    got = oracle.decode16(bits, "bf16")
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+
+
+# -- block-table gather --------------------------------------------------------
+
+def pin_block_ranges_worked_example():
+    """i = 40, B = 16 visits 3 blocks: tokens 1-16, 17-32, 33-40."""
+    g = golden("block_ranges_40_16.json")
+    i, B = g["query_position"], g["block_size"]
+    phys, off = oracle.locate_tokens([0, 1, 2], B, i)
+    assert len(set(phys.tolist())) == g["blocks_visited"]
+    ranges = []
+    for blk in sorted(set(phys.tolist())):
+        toks = np.nonzero(phys == blk)[0] + 1          # 1-based positions
+        ranges.append([int(toks.min()), int(toks.max())])
+        assert np.array_equal(off[phys == blk], np.arange(len(toks)))
+    assert ranges == g["token_ranges_1_based"]
+
+
+def pin_locate_request_flow():
+    """Figure 6: the 8th and 9th tokens of the 7-token prompt's sequence land
+    in physical block 1 offset 3, then physical block 3 offset 0."""
+    phys, off = oracle.locate_tokens([7, 1, 3], 4, 9)
+    assert (phys[7], off[7]) == (1, 3)
+    assert (phys[8], off[8]) == (3, 0)
+    assert phys[:4].tolist() == [7] * 4 and phys[4:8].tolist() == [1] * 4
+
+
+# -- cache write -----------------------------------------------------------------
+
+def pin_cache_write_slot_example():
+    """Slot 12 with B = 4 is block 3, offset 0 (Figure 6, second decode step);
+    nothing else in either cache changes, and a negative slot is skipped."""
+    NB, Hkv, B, d = 6, 2, 4, 8
+    kc0 = _pool(NB, Hkv, B, d, torch.float16, 1)
+    vc0 = _pool(NB, Hkv, B, d, torch.float16, 2)
+    kc, vc = kc0.copy(), vc0.copy()
+    key = _rand16((2, Hkv, d), torch.float16, 3)
+    val = _rand16((2, Hkv, d), torch.float16, 4)
+    oracle.cache_write(key, val, kc, vc, [12, -1])
+    kb, vb = oracle.bits16(key), oracle.bits16(val)
+    assert np.array_equal(kc[3, :, 0, :], kb[0]) and np.array_equal(vc[3, :, 0, :], vb[0])
+    mask = np.ones(kc.shape, bool)
+    mask[3, :, 0, :] = False
+    assert np.array_equal(kc[mask], kc0[mask]) and np.array_equal(vc[mask], vc0[mask])
+
+
+def pin_cache_write_roundtrip():
+    """Tokens written through the slots of an allocated sequence come back,
+    bit for bit, when the sequence is read through its block table."""
+    B, Hkv, d, NB = 8, 3, 16, 40
+    rng = np.random.default_rng(7)
+    alloc = oracle.RefAllocator(NB, B, rng.permutation(NB))
+    sid = alloc.seq_new(0)
+    T = 37
+    slots = [alloc.append(sid)[0] for _ in range(T)]
+    kc = np.zeros((NB, Hkv, B, d), np.uint16)
+    vc = np.zeros_like(kc)
+    key = _rand16((T, Hkv, d), torch.bfloat16, 5)
+    val = _rand16((T, Hkv, d), torch.bfloat16, 6)
+    oracle.cache_write(key, val, kc, vc, slots)
+    phys, off = oracle.locate_tokens(alloc.block_table(sid), B, T)
+    kb, vb = oracle.bits16(key), oracle.bits16(val)
+    for t in range(T):
+        assert np.array_equal(kc[phys[t], :, off[t], :], kb[t])
+        assert np.array_equal(vc[phys[t], :, off[t], :], vb[t])
+    assert int((kc != 0).any(axis=(1, 2, 3)).sum()) <= -(-T // B)
+
+
+# -- block copy ------------------------------------------------------------------
+
+def pin_copy_blocks_exact():
+    """dst := src for every pair, every other block unchanged (a block is all
+    Hkv heads x B tokens x d of one tensor)."""
+    NB, Hkv, B, d = 10, 2, 4, 8
+    c0 = _pool(NB, Hkv, B, d, torch.float16, 9)
+    c = c0.copy()
+    oracle.copy_blocks(c, [(1, 7), (4, 2), (4, 9)])
+    assert np.array_equal(c[7], c0[1]) and np.array_equal(c[2], c0[4]) and np.array_equal(c[9], c0[4])
+    for b in (0, 1, 3, 4, 5, 6, 8):
+        assert np.array_equal(c[b], c0[b])
+
+
+# -- attention -------------------------------------------------------------------
+
+def _sdpa_contiguous(q, kc, vc, ctx, dtype, H, Hkv):
+    """Textbook attention (torch's scaled_dot_product_attention, fp64) over a
+    contiguous copy: with the identity block table, sequence s's tokens are
+    pool blocks s*mb .. s*mb+mb-1 in order."""
+    S = q.shape[0]
+    NB, _, B, d = kc.shape
+    mb = NB // S
+    G = H // Hkv
+    out = np.zeros((S, H, d))
+    for s in range(S):
+        n = int(ctx[s])
+        if n == 0:
+            continue
+        k = kc[s * mb:(s + 1) * mb].to(torch.float64).permute(1, 0, 2, 3).reshape(Hkv, mb * B, d)[:, :n]
+        v = vc[s * mb:(s + 1) * mb].to(torch.float64).permute(1, 0, 2, 3).reshape(Hkv, mb * B, d)[:, :n]
+        k = k.repeat_interleave(G, dim=0)
+        v = v.repeat_interleave(G, dim=0)
+        qq = q[s].to(torch.float64).reshape(H, 1, d)
+        out[s] = F.scaled_dot_product_attention(qq[None], k[None], v[None])[0, :, 0].numpy()
+    return out
+
+
+def pin_attention_vs_sdpa(dtype=torch.float16, H=4, Hkv=2, d=32, B=8, ctx=(1, 5, 8, 9, 23, 40)):
+    """Identity tables: the paged result equals textbook contiguous attention
+    ("the result is identical to attending over one contiguous array")."""
+    S = len(ctx)
+    mb = -(-max(ctx) // B)
+    NB = S * mb
+    q = _rand16((S, H, d), dtype, 11)
+    kc = _rand16((NB, Hkv, B, d), dtype, 12)
+    vc = _rand16((NB, Hkv, B, d), dtype, 13)
+    bt = np.arange(NB, dtype=np.int32).reshape(S, mb)
+    got = oracle.paged_attention(q, kc, vc, bt, np.array(ctx), dtype)
+    want = _sdpa_contiguous(q, kc, vc, ctx, dtype, H, Hkv)
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-14), np.abs(got - want).max()
+
+
+def pin_attention_vs_sdpa_gqa():
+    pin_attention_vs_sdpa(dtype=torch.bfloat16, H=8, Hkv=2, d=16, B=4, ctx=(3, 4, 17, 31))
+
+
+def pin_attention_scale_argument():
+    """An explicit scale multiplies q.k: scale c on q equals scale c on the call."""
+    S, H, d, B = 2, 2, 16, 4
+    ctx = np.array([7, 13])
+    q = _rand16((S, H, d), torch.float16, 21)
+    kc = _rand16((8, H, B, d), torch.float16, 22)
+    vc = _rand16((8, H, B, d), torch.float16, 23)
+    bt = np.arange(8, dtype=np.int32).reshape(2, 4)
+    a = oracle.paged_attention(q, kc, vc, bt, ctx, "f16", scale=0.5 / math.sqrt(d))
+    q2 = (q.to(torch.float64) * 0.5)
+    want = np.zeros_like(a)
+    for s in range(S):
+        k = kc[s * 4:(s + 1) * 4].to(torch.float64).permute(1, 0, 2, 3).reshape(H, 16, d)[:, :ctx[s]]
+        v = vc[s * 4:(s + 1) * 4].to(torch.float64).permute(1, 0, 2, 3).reshape(H, 16, d)[:, :ctx[s]]
+        want[s] = F.scaled_dot_product_attention(q2[s].reshape(H, 1, d)[None], k[None], v[None])[0, :, 0].numpy()
+    assert np.allclose(a, want, rtol=1e-12, atol=1e-14)
+
+
+def pin_permutation_invariance():
+    """Moving the same logical blocks to other physical blocks leaves every
+    output bit-identical (blocks need not be adjacent)."""
+    S, H, Hkv, d, B = 3, 4, 4, 16, 4
+    ctx = np.array([9, 16, 30])
+    mb = 8
+    NB = 40
+    rng = np.random.default_rng(3)
+    q = _rand16((S, H, d), torch.float16, 31)
+    kc = _pool(NB, Hkv, B, d, torch.float16, 32)
+    vc = _pool(NB, Hkv, B, d, torch.float16, 33)
+    bt = rng.permutation(NB)[:S * mb].astype(np.int32).reshape(S, mb)
+    a = oracle.paged_attention(q, kc, vc, bt, ctx, "f16")
+    perm = rng.permutation(NB)          # physical block b moves to perm[b]
+    kc2 = np.empty_like(kc)
+    vc2 = np.empty_like(vc)
+    kc2[perm] = kc
+    vc2[perm] = vc
+    b = oracle.paged_attention(q, kc2, vc2, perm[bt].astype(np.int32), ctx, "f16")
+    assert np.array_equal(a, b)
+
+
+def pin_identical_keys_mean():
+    """All keys equal: the softmax is uniform and the output is the mean of
+    the values (closed form)."""
+    S, H, d, B, n = 1, 1, 8, 4, 11
+    q = _rand16((S, H, d), torch.float16, 41)
+    kc = np.zeros((3, H, B, d), np.uint16)
+    kc[:] = oracle.bits16(_rand16((d,), torch.float16, 42))
+    vc = _pool(3, H, B, d, torch.float16, 43)
+    bt = np.array([[2, 0, 1]], np.int32)
+    got = oracle.paged_attention(q, kc, vc, bt, np.array([n]), "f16")[0, 0]
+    vals = oracle.decode16(vc, "f16")
+    toks = [vals[bt[0, t // B], 0, t % B] for t in range(n)]
+    assert np.allclose(got, np.mean(toks, axis=0), rtol=1e-13, atol=1e-15)
+
+
+def pin_single_token_and_empty():
+    """ctx = 1 returns v_0 exactly; ctx = 0 returns zeros."""
+    q = _rand16((2, 2, 8), torch.bfloat16, 51)
+    kc = _pool(4, 2, 4, 8, torch.bfloat16, 52)
+    vc = _pool(4, 2, 4, 8, torch.bfloat16, 53)
+    bt = np.array([[3, 0], [1, 2]], np.int32)
+    got = oracle.paged_attention(q, kc, vc, bt, np.array([1, 0]), "bf16")
+    v = oracle.decode16(vc, "bf16")
+    assert np.array_equal(got[0, 0], v[3, 0, 0]) and np.array_equal(got[0, 1], v[3, 1, 0])
+    assert np.array_equal(got[1], np.zeros((2, 8)))
+
+
+def pin_one_hot_limit():
+    """One key much better aligned with q than the others takes (nearly) all
+    the weight: the output tends to that token's value."""
+    d, B, n = 16, 4, 10
+    q = torch.zeros(1, 1, d, dtype=torch.float16)
+    q[0, 0, 5] = 8.0
+    kc = np.zeros((3, 1, B, d), np.uint16)
+    j = 6                                          # logical token 6 -> block bt[1], offset 2
+    bt = np.array([[1, 2, 0]], np.int32)
+    kbits = torch.zeros(d, dtype=torch.float16)
+    kbits[5] = 8.0
+    kc[bt[0, j // B], 0, j % B] = oracle.bits16(kbits)
+    vc = _pool(3, 1, B, d, torch.float16, 61)
+    got = oracle.paged_attention(q, kc, vc, bt, np.array([n]), "f16")[0, 0]
+    want = oracle.decode16(vc, "f16")[bt[0, j // B], 0, j % B]
+    # weight of the others is (n-1) e^{-16} relative: under 1e-5
+    assert np.allclose(got, want, rtol=0, atol=1e-5 * (1 + np.abs(want).max()))
+
+
+def pin_which_subset():
+    """Computing a subset of (s, h) gives exactly the rows of the full call."""
+    S, H, Hkv, d, B = 3, 4, 2, 8, 4
+    ctx = np.array([5, 12, 3])
+    q = _rand16((S, H, d), torch.float16, 71)
+    kc = _pool(12, Hkv, B, d, torch.float16, 72)
+    vc = _pool(12, Hkv, B, d, torch.float16, 73)
+    bt = np.arange(12, dtype=np.int32).reshape(3, 4)
+    full = oracle.paged_attention(q, kc, vc, bt, ctx, "f16")
+    part = oracle.paged_attention(q, kc, vc, bt, ctx, "f16", which=[(2, 3), (0, 1)])
+    assert np.array_equal(part[2, 3], full[2, 3]) and np.array_equal(part[0, 1], full[0, 1])
+    assert np.isnan(part[1]).all()
+
+
+# -- split context -----------------------------------------------------------------
+
+def pin_partition_merge_identity():
+    """Splitting the context into partitions and merging by log-sum-exp gives
+    the unsplit result (equal in exact arithmetic)."""
+    S, H, Hkv, d, B = 2, 4, 1, 16, 8
+    ctx = np.array([1000, 517])
+    mb = 128
+    NB = S * mb
+    q = _rand16((S, H, d), torch.bfloat16, 81)
+    kc = _pool(NB, Hkv, B, d, torch.bfloat16, 82)
+    vc = _pool(NB, Hkv, B, d, torch.bfloat16, 83)
+    bt = np.random.default_rng(8).permutation(NB).astype(np.int32).reshape(S, mb)
+    full = oracle.paged_attention(q, kc, vc, bt, ctx, "bf16")
+    for P in (16, 96, 512, 4096):
+        for s in range(S):
+            for h in range(H):
+                m, l, o = oracle.partition_stats(q, kc, vc, bt, ctx, "bf16", s, h, P)
+                assert len(m) == -(-int(ctx[s]) // P)
+                got = oracle.merge_partitions(m, l, o)
+                assert np.allclose(got, full[s, h], rtol=1e-12, atol=1e-14)
+
+
+def pin_partition_stats_definition():
+    """A single partition's (m, l, o) are the max score, the sum of
+    exp(score - m) and the un-normalised value sum, computed directly."""
+    d, B = 8, 4
+    q = _rand16((1, 1, d), torch.float16, 91)
+    kc = _pool(4, 1, B, d, torch.float16, 92)
+    vc = _pool(4, 1, B, d, torch.float16, 93)
+    bt = np.array([[2, 3, 0, 1]], np.int32)
+    m, l, o = oracle.partition_stats(q, kc, vc, bt, np.array([14]), "f16", 0, 0, 8)
+    K = oracle.decode16(kc, "f16")
+    V = oracle.decode16(vc, "f16")
+    qq = q.to(torch.float64).numpy()[0, 0]
+    for p, (t0, t1) in enumerate([(0, 8), (8, 14)]):
+        ks = np.array([K[bt[0, t // B], 0, t % B] for t in range(t0, t1)])
+        vs = np.array([V[bt[0, t // B], 0, t % B] for t in range(t0, t1)])
+        x = ks @ qq / math.sqrt(d)
+        assert np.isclose(m[p], x.max(), rtol=1e-14)
+        w = np.exp(x - x.max())
+        assert np.isclose(l[p], w.sum(), rtol=1e-13)
+        assert np.allclose(o[p], w @ vs, rtol=1e-12, atol=1e-14)
+
+
+# -- sizes from the pages -------------------------------------------------------------
+
+def pin_kv_size():
+    g = golden("kv_size_opt13b.json")
+    per = oracle.kv_bytes_per_token(g["hidden"], g["layers"], g["bytes_per_number"])
+    assert per == g["per_token_bytes"]
+    assert per / 1024 == g["per_token_kb"]
+    assert round(g["request_tokens"] * per / 1024 / 1e6, 1) == g["request_gb_rounded"]
+
+
+def pin_capacity():
+    g = golden("capacity_13b.json")
+    slots = g["kv_memory_gib"] * 2 ** g["kv_memory_bytes_exponent"] / (g["per_token_kb"] * 1024)
+    assert round(slots / 1000, 1) == g["max_slots_thousands_rounded"]
+
+
+def pin_waste_example():
+    g = golden("waste_100_200.json")
+    used = g["prompt_tokens"] + g["output_tokens"]
+    assert used == g["used_slots"]
+    assert g["reservation_tokens"] - used == g["reservation_waste_slots"]
+    assert round(100 * (g["reservation_tokens"] - used) / g["reservation_tokens"]) == \
+        g["reservation_waste_percent_rounded"]
+    n = oracle.blocks_needed(used, g["block_size"])
+    assert n == g["blocks"] and n * g["block_size"] == g["block_slots"]
+    assert n * g["block_size"] - used == g["block_waste_slots"]
+    a = oracle.RefAllocator(32, g["block_size"])
+    sid = a.seq_new(g["prompt_tokens"])
+    for _ in range(g["output_tokens"]):
+        a.append(sid)
+    assert len(a.block_table(sid)) == g["blocks"]
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -1,0 +1,66 @@
+"""Plant plausible mistakes in copies of the oracle's C source and check that
+the pins catch every one (CPU only).  The oracle under test is never edited;
+each mutant is compiled to a temporary library and swapped in for the run."""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "pkv_oracle.c")
+
+# (name, text to replace, replacement, which occurrence (0-based))
+MUTANTS = [
+    ("scale dropped", "x[t - t0] = scale * dot;", "x[t - t0] = dot;", 0),
+    ("gqa map modulo", "int g = h / (H / Hkv);", "int g = h % Hkv;", 0),
+    ("offset shifted", "*off = (int32_t)(t % B);", "*off = (int32_t)((t + 1) % B);", 0),
+    ("logical block used as physical", "*phys = table_row[t / B];", "*phys = (int32_t)(t / B);", 0),
+    ("no normalisation", "o[i] = l > 0.0 ? o[i] / l : 0.0;", "o[i] = l > 0.0 ? o[i] : 0.0;", 0),
+    ("value read from key cache", "const uint16_t *v = value_cache +", "const uint16_t *v = key_cache +", 0),
+    ("last token dropped from PV", "for (int64_t t = t0; t < t1; t++) {", "for (int64_t t = t0; t + 1 < t1; t++) {", 1),
+    ("half exponent bias", "e - 15 - 10", "e - 14 - 10", 0),
+    ("half subnormal scale", "ldexp((double)f, -24)", "ldexp((double)f, -25)", 0),
+    ("bfloat16 shift", "(uint32_t)b << 16", "(uint32_t)b << 15", 0),
+    ("cache write offset", "int64_t blk = s / B, off = s % B;", "int64_t blk = s / B, off = (s + 1) % B;", 0),
+    ("negative slot not skipped", "if (s < 0)\n            continue;", "if (s < -1)\n            continue;", 0),
+    ("copy direction swapped",
+     "cache[(int64_t)dst * block_elems + i] = cache[(int64_t)src * block_elems + i];",
+     "cache[(int64_t)src * block_elems + i] = cache[(int64_t)dst * block_elems + i];", 0),
+    ("merge ignores partition weight", "L += l[p] * w;", "L += l[p];", 0),
+    ("partition end off by one", "int64_t t1 = t0 + P < ctx ? t0 + P : ctx;",
+     "int64_t t1 = t0 + P < ctx ? t0 + P - 1 : ctx;", 0),
+    ("max not tracked", "if (x[t - t0] > m)\n            m = x[t - t0];", "if (x[t - t0] > m)\n            m = 0.0;", 0),
+]
+
+
+def _replace_nth(text, old, new, n):
+    idx = -1
+    for _ in range(n + 1):
+        idx = text.index(old, idx + 1)
+    return text[:idx] + new + text[idx + len(old):]
+
+
+@pytest.mark.parametrize("name,old,new,nth", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, name, old, new, nth):
+    src = open(SRC).read()
+    mutated = _replace_nth(src, old, new, nth)
+    assert mutated != src
+    c = tmp_path / "mutant.c"
+    so = tmp_path / "libmutant.so"
+    c.write_text(mutated)
+    subprocess.run(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fPIC", "-shared",
+                    "-o", str(so), str(c), "-lm"], check=True)
+    saved = oracle._lib
+    oracle._lib = oracle.load(so)
+    failed = []
+    try:
+        for pin in pins.ALL_PINS:
+            try:
+                pin()
+            except (AssertionError, ValueError):
+                failed.append(pin.__name__)
+    finally:
+        oracle._lib = saved
+    assert failed, f"no pin caught the planted mistake: {name}"
