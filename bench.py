@@ -1,0 +1,386 @@
+"""Benchmark of the paged decode hot path on GB300.
+
+One step = one decode iteration of one layer over the whole batch: the
+copy-on-write block copies (if the step has any), the slot-mapped write of
+the batch's new keys and values, and paged decode attention over every
+sequence's block table (including the partition merge).  Host allocation is
+done once before timing.  The metric is effective KV-read bandwidth:
+sum over sequences of context_len x 2 x kv_heads x head_dim x 2 bytes,
+divided by the step time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload opt13b]
+                    [--block-size B] [--partition-size P] [--impl reference]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs an independent
+replica (a different seed) on its own GPU; the value is all ranks' bytes over
+the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import pathlib
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = pathlib.Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+import workloads  # noqa: E402
+
+METRIC = "paged decode attention effective KV-read GB/s and % of GB300 HBM peak"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="opt13b", choices=["tiny", "opt13b", "llama7b", "sampling", "longgqa"])
+    ap.add_argument("--block-size", type=int, default=16)
+    ap.add_argument("--partition-size", type=int, default=-1)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def make_workload(args, rank: int) -> workloads.Workload:
+    kw = {}
+    if args.workload == "llama7b":
+        kw["block_size"] = args.block_size
+    w = workloads.by_name(args.workload, **kw)
+    if rank:
+        w = workloads.by_name(args.workload, seed=w.seed + 7919 * rank, **kw) if args.workload != "tiny" else w
+    if args.partition_size >= 0:
+        w.partition_size = args.partition_size
+    return w
+
+
+# -- measured peaks and profile figures --------------------------------------------
+
+def hbm_peak():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            d = json.loads(p.read_text())
+            for k in ("hbm_gbs", "hbm_GBps", "hbm"):
+                if k in d and d[k]:
+                    return float(d[k]), "measured"
+        except (ValueError, TypeError):
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def profile_traffic(workload_name: str):
+    """DRAM bytes per launch of the attention kernel from a committed ncu
+    summary (a line 'traffic_bytes_per_launch[<workload>]: N'), else None."""
+    for f in sorted((ROOT / "profiles").glob("*.md")):
+        for line in f.read_text().splitlines():
+            key = f"traffic_bytes_per_launch[{workload_name}]:"
+            if line.strip().startswith(key):
+                try:
+                    return float(line.split(":", 1)[1].split()[0])
+                except ValueError:
+                    return None
+    return None
+
+
+# -- clocks ------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = "index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active," \
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown," \
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap"
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# -- the CPU baseline (the oracle as it stands) -------------------------------------
+
+def cpu_baseline(w: workloads.Workload, t: dict, tables: np.ndarray, ctx: np.ndarray, slots, budget_s=12.0):
+    import oracle
+    kc = oracle.bits16(t["key_cache"])
+    vc = oracle.bits16(t["value_cache"])
+    oracle.cache_write(t["key"], t["value"], kc, vc, slots)
+    q = t["query"].cpu()
+    bpt = w.kv_bytes_per_token // w.num_kv_heads          # K+V bytes of one token of one kv head
+    G = w.num_heads // w.num_kv_heads
+    # a bounded sample: whole sequences, in order, until about budget_s of CPU time
+    done_bytes, t0, seqs = 0, time.perf_counter(), 0
+    order = np.random.default_rng(w.seed).permutation(w.num_seqs)
+    for s in order:
+        which = [(int(s), h) for h in range(w.num_heads)]
+        oracle.paged_attention(q, kc, vc, tables, ctx, w.dtype, which=which)
+        done_bytes += int(ctx[s]) * bpt * w.num_kv_heads      # every kv head's K and V read once
+        seqs += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": done_bytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{seqs} of {w.num_seqs} sequences, all {w.num_heads} heads (G={G}), fp64, single thread, "
+                      f"{dt:.1f} s"}
+
+
+def run_reference(args, rank: int, world: int):
+    if rank != 0:
+        return
+    w = make_workload(args, 0)
+    t = workloads.tensors(w, "cpu")
+    import oracle
+    ref = oracle.RefAllocator(w.num_blocks, w.block_size, workloads.free_order(w.num_blocks, w.seed))
+    ids = [ref.seq_new(int(c) - 1) for c in w.context_lens] if w.prompt_lens is None else None
+    if ids is None:
+        print(json.dumps({"impl": "reference", "unavailable": "reference arm runs the tiny/opt13b/llama7b/longgqa "
+                          "workloads only"}))
+        return
+    slots, _ = ref.append_batch(ids)
+    tables = np.full((len(ids), w.max_blocks_per_seq), -1, np.int32)
+    for i, sid in enumerate(ids):
+        bt = ref.block_table(sid)
+        tables[i, :len(bt)] = bt
+    ctx = np.array([ref.seq_len(s) for s in ids], np.int32)
+    per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    vals = []
+    for i in range(args.warmup + args.steps):
+        cb = cpu_baseline(w, t, tables, ctx, slots, budget_s=per_step)
+        if i >= args.warmup:
+            vals.append(cb)
+    v = statistics.median([c["value"] for c in vals])
+    total_bytes = int(ctx.sum()) * w.kv_bytes_per_token
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_bytes / (v * 1e9) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {**w.describe(), "kernel": "oracle (fp64 C, CPU)"},
+            "cpu_baseline": {**vals[-1], "value": v},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+# -- our arm -----------------------------------------------------------------------------
+
+def run_ours(args, rank: int, world: int):
+    import paged_kv_cache_139_gb300 as pkv
+    from paged_kv_cache_139_gb300.engine import PagedKVCache
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w = make_workload(args, rank)
+    if w.prompt_lens is not None:
+        raise SystemExit("bench: the sampling workload is measured by its tests and the copy benchmark")
+    t_gpu = workloads.tensors(w, device=dev)
+    order = workloads.free_order(w.num_blocks, w.seed)
+    eng = PagedKVCache(w.num_blocks, w.num_kv_heads, w.head_dim, w.block_size, w.torch_dtype, dev,
+                       w.max_blocks_per_seq, order, key_cache=t_gpu["key_cache"], value_cache=t_gpu["value_cache"])
+    ids = [eng.new_sequence(int(c) - 1) for c in w.context_lens]
+    plan = eng.plan_step(ids)
+    step = eng.upload(plan)
+    q, key, value = t_gpu["query"], t_gpu["key"], t_gpu["value"]
+    out = torch.empty_like(q)
+    P = w.partition_size
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    kv_bytes = int(plan.context_lens.astype(np.int64).sum()) * w.kv_bytes_per_token
+
+    def device_step():
+        eng.decode(q, key, value, step, out=out, partition_size=P)
+
+    # warm-up (also checks that the step runs clean)
+    for _ in range(args.warmup):
+        flush.zero_()
+        device_step()
+    pkv.check()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = pkv.launch_count()
+    with ClockSampler(dev.index) as clk:
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()                                     # L2 flushed before every step
+            starts[i].record(stream)
+            eng.copy_on_write(step.pairs)
+            eng.write(key, value, step.slots)
+            mids[i].record(stream)
+            eng.attend(q, step, out=out, partition_size=P)
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - wall0
+    if dist:
+        dist.barrier()
+    launches = pkv.launch_count() - launches0
+    pkv.check()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    attn_ms = [m.elapsed_time(e) for m, e in zip(mids, ends)]
+    t_step = sum(step_ms) / len(step_ms)
+    t_attn = sum(attn_ms) / len(attn_ms)
+
+    # paged vs contiguous placement of the same batch (identity block tables)
+    nblk = -(-plan.context_lens.astype(np.int64) // w.block_size)
+    ident = np.full_like(plan.tables, -1)
+    base = 0
+    for i, n in enumerate(nblk):
+        ident[i, :n] = np.arange(base, base + n)
+        base += n
+    ident_dev = torch.from_numpy(ident).to(dev)
+    istep = type(step)(step.slots, step.pairs, ident_dev, step.context_lens, step.max_context_len)
+    contig = []
+    for i in range(max(3, args.steps // 2)):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        eng.attend(q, istep, out=torch.empty_like(out), partition_size=P)
+        b.record(stream)
+        contig.append((a, b))
+    torch.cuda.synchronize(dev)
+    t_contig = statistics.median([a.elapsed_time(b) for a, b in contig])
+    pkv.check()
+
+    # end to end through the public API from pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        h = {n: x.cpu().pin_memory() for n, x in (("q", q), ("key", key), ("value", value))}
+        h["slots"] = torch.from_numpy(plan.slots).pin_memory()
+        h["tables"] = torch.from_numpy(plan.tables).pin_memory()
+        h["ctx"] = torch.from_numpy(plan.context_lens).pin_memory()
+        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        d = {n: torch.empty_like(x, device=dev) for n, x in h.items()}
+        dstep = type(step)(d["slots"], step.pairs, d["tables"], d["ctx"], step.max_context_len)
+        h2d = sum(x.numel() * x.element_size() for x in h.values())
+        d2h = h_out.numel() * h_out.element_size()
+        times = []
+        for i in range(args.warmup + args.steps):
+            flush.zero_()
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            for n in h:
+                d[n].copy_(h[n], non_blocking=True)
+            eng.decode(d["q"], d["key"], d["value"], dstep, out=out, partition_size=P)
+            h_out.copy_(out, non_blocking=True)
+            torch.cuda.synchronize(dev)
+            if i >= args.warmup:
+                times.append(time.perf_counter() - t0)
+        t_e2e = sum(times) / len(times)
+        e2e = {"value": kv_bytes / t_e2e / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3}
+        pkv.check()
+
+    # the slowest rank sets the time
+    t_step_max = t_step
+    total_bytes = kv_bytes
+    if dist:
+        x = torch.tensor([t_step, float(kv_bytes)], dtype=torch.float64, device=dev)
+        y = x.clone()
+        dist.all_reduce(x[:1], op=dist.ReduceOp.MAX)
+        dist.all_reduce(y[1:], op=dist.ReduceOp.SUM)
+        t_step_max, total_bytes = float(x[0]), float(y[1])
+    if rank != 0:
+        return
+
+    peak, peak_src = hbm_peak()
+    value = total_bytes / (t_step_max * 1e-3) / 1e9
+    attn_gbs = kv_bytes / (t_attn * 1e-3) / 1e9
+    traffic = profile_traffic(args.workload if args.workload != "llama7b" else f"llama7b_B{w.block_size}")
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_step_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "kv_dtype": w.dtype, "data": "synthetic",
+        "config": {**w.describe(), "partition_size": pkv.paged_attention_partition_size(
+            w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim, step.max_context_len, P),
+            "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB memset, outside the timed events)",
+            "kv_bytes_per_step": kv_bytes, "parallelism": f"replicas x{world}"},
+        "pct_of_hbm_peak": 100.0 * value / world / peak,
+        "tokens_per_s": w.num_seqs * world / (t_step_max * 1e-3),
+        "roofline": {"bound": "hbm", "achieved": attn_gbs, "peak": peak, "unit": "GB/s", "frac": attn_gbs / peak,
+                     "traffic": traffic, "kernel": "paged_attention_decode (partition kernel + merge)",
+                     "peak_source": f"{peak_src} {'MEASURED_PEAKS.json hbm_gbs' if peak_src == 'measured' else '6.8 TB/s'}",
+                     "ms_per_launch": t_attn},
+        "paged_overhead": {"contiguous_ms": t_contig, "paged_ms": t_attn,
+                           "slowdown_pct": 100.0 * (t_attn / t_contig - 1.0)},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": wall,
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline:
+        t_cpu = workloads.tensors(w, "cpu")
+        line["cpu_baseline"] = cpu_baseline(w, t_cpu, plan.tables, plan.context_lens, plan.slots)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,236 @@
+/*
+ * pkv.h -- C ABI of libpkv: the decode hot path of PagedAttention on GB300.
+ *
+ * The operations follow the statement of the problem in "vLLM &
+ * PagedAttention: Efficient Memory Management for LLM Serving" (§III
+ * blockwise attention, §V request flow, §VII sharing and copy-on-write, §X
+ * the three fused kernels and the fork/append/free primitives) and
+ * "PagedAttention and vLLM, annotated" (§4.1 blockwise attention, §4.2 block
+ * tables, §4.4 copy-on-write).
+ *
+ * Conventions for every call:
+ *   - Returns pkv_status; PKV_OK is 0.  On failure pkv_last_error_string()
+ *     describes the last error of the calling thread.
+ *   - Pointers named *_dev are device pointers; the caller owns all device
+ *     memory (the library allocates none for these calls) and must keep it
+ *     alive until the work on `stream` has finished.  Device pointers must be
+ *     16-byte aligned.
+ *   - Device work is asynchronous on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream).  Arguments are checked on the host before any
+ *     launch; a bad argument returns PKV_EINVAL and launches nothing.
+ *   - Index errors that only the device can see (a slot or block id outside
+ *     the pool, a context longer than its table) are latched in a per-device
+ *     status word; the offending access is skipped and the affected outputs
+ *     are unspecified.  pkv_check() synchronises `stream`, reports the
+ *     latched error (PKV_EINDEX, or PKV_ETIMEOUT when a bounded device-side
+ *     wait gave up) and clears it.  Device errors are never raised with
+ *     traps or asserts: the CUDA context stays usable.
+ *   - 16-bit data are fp16 or bf16 (pkv_dtype); the library copies their bit
+ *     patterns and computes in fp32.
+ *
+ * Layouts (row-major, innermost last):
+ *   key_cache, value_cache   [num_blocks][num_kv_heads][block_size][head_dim]
+ *   key, value (new tokens)  [num_tokens][num_kv_heads][head_dim]
+ *   query, out               [num_seqs][num_heads][head_dim]
+ *   block_tables             [num_seqs][max_blocks_per_seq] int32
+ *   context_lens             [num_seqs] int32 (includes the decode token)
+ * Query head h reads kv head h / (num_heads / num_kv_heads).
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;                       /* cudaStream_t is struct CUstream_st* */
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_EINVAL = 1,    /* bad argument; nothing was launched */
+    PKV_ENOMEM = 2,    /* allocator: too few free blocks; state unchanged */
+    PKV_EINDEX = 3,    /* device saw an index outside the pool or table */
+    PKV_ECUDA = 4,     /* a CUDA runtime call failed */
+    PKV_ETIMEOUT = 5   /* a bounded device-side wait gave up */
+} pkv_status;
+
+typedef enum pkv_dtype { PKV_F16 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+/* ---------------------------------------------------------------------------
+ * kv_reshape_and_cache -- the fused reshape + block write ("vLLM &
+ * PagedAttention" §X, first kernel; §V steps 2-3).
+ *
+ * For each token t with s = slot_mapping[t] >= 0: block b = s / block_size,
+ * offset o = s % block_size, and for every kv head h
+ *   key_cache[b][h][o][:] = key[t][h][:],  value_cache[b][h][o][:] = value[t][h][:]
+ * copied bit for bit.  A negative slot marks a padding token and is skipped.
+ * A slot >= num_blocks * block_size latches PKV_EINDEX and is skipped.
+ * Slots must be distinct (two tokens with one slot race).
+ *   key_dev, value_dev           [num_tokens][num_kv_heads][head_dim] 16-bit
+ *   key_cache_dev, value_cache_dev  the pool, see Layouts
+ *   slot_mapping_dev             [num_tokens] int64
+ * head_dim must be a multiple of 8; block_size a power of two; num_tokens
+ * may be 0 (nothing launched).
+ * ------------------------------------------------------------------------- */
+pkv_status kv_reshape_and_cache(const void *key_dev, const void *value_dev,
+                                void *key_cache_dev, void *value_cache_dev,
+                                const int64_t *slot_mapping_dev, int num_tokens,
+                                int num_kv_heads, int head_dim, int block_size,
+                                int num_blocks, pkv_dtype dtype, struct CUstream_st *stream);
+
+/* ---------------------------------------------------------------------------
+ * paged_attention_decode -- block-table gather + decode attention ("vLLM &
+ * PagedAttention" §I attention equation, §III blockwise equation, §X second
+ * kernel; "PagedAttention and vLLM, annotated" §4.1).
+ *
+ * For every sequence s and query head h, with g = h / (num_heads/num_kv_heads)
+ * and n = context_lens[s]:
+ *   x_t = scale * query[s][h] . K_t,   K_t = key_cache[block_tables[s][t / B]][g][t % B]
+ *   out[s][h] = sum_{t<n} softmax(x)_t * V_t          (V_t likewise)
+ * rounded to `dtype`.  n = 0 gives zeros.  scale is usually 1/sqrt(head_dim).
+ *
+ * Long contexts are split into partitions of partition_size tokens; each is
+ * reduced to (max, sum of exponentials, un-normalised value sum) and a second
+ * kernel merges them by log-sum-exp.  partition_size = 0 lets the library
+ * choose; otherwise it must be a positive multiple of 32.
+ *   max_context_len   host-side upper bound on every context_lens[s]
+ *                     (0 = max_blocks_per_seq * block_size); a larger
+ *                     context latches PKV_EINDEX.
+ *   num_blocks        pool size; a table entry outside [0, num_blocks)
+ *                     within a context latches PKV_EINDEX.  Entries past
+ *                     ceil(n / B) are never read.
+ *   workspace_dev     at least paged_attention_workspace_size(...) bytes of
+ *                     device scratch owned by the caller (may be NULL when
+ *                     that size is 0); its contents need no initialisation
+ *                     and are clobbered.
+ * head_dim in {64, 128}; block_size a power of two in [4, 128];
+ * num_heads % num_kv_heads == 0.
+ * ------------------------------------------------------------------------- */
+pkv_status paged_attention_decode(void *out_dev, const void *query_dev,
+                                  const void *key_cache_dev, const void *value_cache_dev,
+                                  const int32_t *block_tables_dev,
+                                  const int32_t *context_lens_dev, int num_seqs,
+                                  int max_blocks_per_seq, int max_context_len,
+                                  int block_size, int num_blocks, int num_heads,
+                                  int num_kv_heads, int head_dim, float scale,
+                                  int partition_size, void *workspace_dev,
+                                  size_t workspace_bytes, pkv_dtype dtype,
+                                  struct CUstream_st *stream);
+
+/* Bytes of workspace paged_attention_decode needs for these sizes (0 when no
+ * context can span more than one partition).  partition_size as above. */
+size_t paged_attention_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
+                                      int head_dim, int max_context_len,
+                                      int partition_size);
+
+/* The partition size paged_attention_decode uses for these arguments. */
+int paged_attention_partition_size(int num_seqs, int num_heads, int num_kv_heads,
+                                   int head_dim, int max_context_len, int partition_size);
+
+/* ---------------------------------------------------------------------------
+ * copy_blocks -- the fused block copy for copy-on-write ("vLLM &
+ * PagedAttention" §X, third kernel; §VII Figure 8).
+ *
+ * For each pair p: block dst = src_dst_pairs[2p+1] of `cache` becomes a copy
+ * of block src = src_dst_pairs[2p], block_bytes bytes each (for the layout
+ * above, block_bytes = num_kv_heads * block_size * head_dim * 2).  Call once
+ * for the key cache and once for the value cache.
+ *   cache_dev          [num_blocks] blocks of block_bytes bytes
+ *   src_dst_pairs_dev  [num_pairs][2] int32, device memory
+ * block_bytes must be a positive multiple of 16.  A block id outside
+ * [0, num_blocks) latches PKV_EINDEX and that pair is skipped.  Destinations
+ * must be distinct and no destination may also be a source (the pairs an
+ * allocator's copy-on-write produces always are); pkv_validate_copy_pairs
+ * checks this on a host copy.  num_pairs may be 0 (nothing launched).
+ * ------------------------------------------------------------------------- */
+pkv_status copy_blocks(void *cache_dev, const int32_t *src_dst_pairs_dev, int num_pairs,
+                       int64_t block_bytes, int num_blocks, struct CUstream_st *stream);
+
+/* Host-side check of a pair list: ids in range, distinct destinations, no
+ * destination that is also a source.  PKV_EINVAL if any fails. */
+pkv_status pkv_validate_copy_pairs(const int32_t *src_dst_pairs_host, int num_pairs,
+                                   int num_blocks);
+
+/* ---------------------------------------------------------------------------
+ * Status and introspection
+ * ------------------------------------------------------------------------- */
+
+/* Synchronise `stream`, then report and clear the error latched on the
+ * current device (PKV_OK, PKV_EINDEX or PKV_ETIMEOUT; PKV_ECUDA when the
+ * stream itself failed). */
+pkv_status pkv_check(struct CUstream_st *stream);
+
+/* Message for the last failing call of this thread (never NULL). */
+const char *pkv_last_error_string(void);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t pkv_launch_count(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int pkv_version(void);
+
+/* Self-test of the bounded device-side wait: launches one CTA that waits on
+ * an mbarrier nothing ever arrives on, for at most limit_cycles clock
+ * cycles (0 < limit_cycles <= 2^32).  The wait gives up, latches the timeout
+ * and the kernel returns, so that a later pkv_check reports PKV_ETIMEOUT and
+ * the context stays usable.  No counterpart on the pages: it exercises the
+ * library's failure path without faulting or hanging the GPU. */
+pkv_status pkv_selftest_wait_timeout(long long limit_cycles, struct CUstream_st *stream);
+
+/* ---------------------------------------------------------------------------
+ * Host block allocator ("vLLM & PagedAttention" §V, §VII, §X; "How
+ * PagedAttention changed LLM serving throughput": a sequence uses exactly
+ * ceil(len / block_size) blocks).
+ *
+ * A pool of num_blocks physical blocks with a reference count each.  Blocks
+ * are handed out in the order `free_order` lists (a permutation of
+ * 0..num_blocks-1; NULL = ascending); freed blocks are pushed back in the
+ * freed sequence's logical order and handed out again last-in, first-out.
+ * Sequence ids are assigned 0, 1, 2, ... in creation order and never reused.
+ * A call that returns PKV_ENOMEM leaves the allocator unchanged.  The
+ * allocator is not thread-safe; it makes no CUDA calls.
+ * ------------------------------------------------------------------------- */
+typedef struct pkv_allocator pkv_allocator;
+
+pkv_status pkv_alloc_create(int num_blocks, int block_size, const int32_t *free_order,
+                            pkv_allocator **out);
+void pkv_alloc_destroy(pkv_allocator *a);
+
+/* A new sequence of len tokens holding ceil(len / block_size) fresh blocks. */
+pkv_status pkv_seq_new(pkv_allocator *a, int64_t len, int32_t *seq);
+/* A new sequence sharing every block of `seq` (each count + 1). */
+pkv_status pkv_seq_fork(pkv_allocator *a, int32_t seq, int32_t *child);
+/* Add one token.  A full (or absent) last block gets a fresh block appended;
+ * a shared (count > 1) partly filled last block is replaced by a fresh block
+ * and (cow_src, cow_dst) = (old, new) is returned for copy_blocks, else both
+ * are -1.  *slot = table[len / B] * B + len % B for the token's position. */
+pkv_status pkv_seq_append(pkv_allocator *a, int32_t seq, int64_t *slot, int32_t *cow_src,
+                          int32_t *cow_dst);
+/* One token for each of seqs[0..n-1] in order (all or nothing).  slots[n];
+ * cow_pairs has room for n pairs; *num_pairs receives the count. */
+pkv_status pkv_seq_append_batch(pkv_allocator *a, const int32_t *seqs, int n, int64_t *slots,
+                                int32_t *cow_pairs, int *num_pairs);
+/* Drop the sequence; blocks whose count reaches 0 return to the pool. */
+pkv_status pkv_seq_free(pkv_allocator *a, int32_t seq);
+pkv_status pkv_seq_len(const pkv_allocator *a, int32_t seq, int64_t *len);
+/* Copy the block table (at most cap entries) and its length. */
+pkv_status pkv_seq_block_table(const pkv_allocator *a, int32_t seq, int32_t *out, int cap,
+                               int *n);
+/* Fill tables[n][max_blocks] (unused entries -1) and context_lens[n] for a
+ * batch of sequences, ready to upload for paged_attention_decode. */
+pkv_status pkv_build_block_tables(const pkv_allocator *a, const int32_t *seqs, int n,
+                                  int32_t *tables, int max_blocks, int32_t *context_lens);
+/* Reference count of a block (-1 if out of range). */
+int pkv_block_ref(const pkv_allocator *a, int32_t block);
+int pkv_num_free(const pkv_allocator *a);
+/* Free blocks in the order they would be handed out (at most cap). */
+pkv_status pkv_free_list(const pkv_allocator *a, int32_t *out, int cap, int *n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -1,0 +1,545 @@
+// Paged decode attention: block-table gather, QK scores, online softmax, PV,
+// split into context partitions with a log-sum-exp merge.
+//
+// What it computes ("vLLM & PagedAttention: Efficient Memory Management for
+// LLM Serving", §I attention equation and §III blockwise equation;
+// "PagedAttention and vLLM, annotated" §4.1): for each sequence s and query
+// head h, out = sum_t softmax_t(scale * q . k_t) v_t over the sequence's
+// context, where token t lives in physical block block_tables[s][t / B] at
+// offset t % B.  The result equals attention over a contiguous array.
+//
+// How (sm_103a):
+//   * One CTA per (kv head x query-head tile, sequence, context partition).
+//     A partition is P tokens (a multiple of 32); a sequence with one
+//     partition writes its output directly, otherwise the CTA writes its
+//     partition's (max, sum of exponentials, un-normalised PV) and a second
+//     kernel merges the partitions.
+//   * A producer warp walks the block table (32 entries per coalesced load)
+//     and streams each 32-token stage of K and V -- whole blocks, or a
+//     32-token slice of a larger block, contiguous in the cache layout
+//     [NB][Hkv][B][d] -- into a shared-memory ring with 1-D bulk TMA copies
+//     completing on mbarriers.
+//   * Four consumer warps take stages round-robin.  In a stage each lane
+//     holds a 16-byte chunk of a row (d/8 lanes per row); QK partial dots are
+//     combined by a butterfly reduce-scatter so that each lane ends with the
+//     score of one token; the online softmax keeps a running max and sum per
+//     head in fp32 (log2 domain); PV accumulates fp32 per lane.  At the end
+//     the four warps' states are merged through shared memory.
+//   * All mbarrier waits are bounded; a wait that gives up latches a timeout
+//     in the status word and the kernel drains its copies and returns.
+#include <cfloat>
+
+#include "pkv_host.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kStageRows = 32;              // tokens per ring stage
+constexpr unsigned kFull = 0xffffffffu;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D> struct Geometry {
+    static constexpr int LPR = D / 8;       // lanes per row (16 bytes each)
+    static constexpr int RPI = 32 / LPR;    // rows covered by one warp-wide load
+    static constexpr int NI = kStageRows / RPI;   // loads per stage (== LPR)
+    static constexpr int NSTAGE = D >= 128 ? 6 : 8;
+    static constexpr int STAGE_ELEMS = kStageRows * D;   // per tensor
+};
+
+template <int D, typename T> constexpr size_t smem_bytes() {
+    using Gm = Geometry<D>;
+    return (size_t)Gm::NSTAGE * 2 * Gm::STAGE_ELEMS * sizeof(T) + Gm::NSTAGE * 2 * sizeof(uint64_t) +
+           Gm::NSTAGE * sizeof(int);
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) x = fmaxf(x, __shfl_xor_sync(kFull, x, o));
+    return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
+    return x;
+}
+
+// v[0..N-1] held by each of N consecutive lanes (lane index c within the
+// group).  Returns, on lane c, the sum over the group of v[c].
+template <int N> __device__ __forceinline__ float reduce_scatter(float (&v)[N], int c) {
+#pragma unroll
+    for (int m = N / 2; m >= 1; m >>= 1) {
+        const bool upper = (c & m) != 0;
+#pragma unroll
+        for (int j = 0; j < m; j++) {
+            const float send = upper ? v[j] : v[j + m];
+            const float keep = upper ? v[j + m] : v[j];
+            v[j] = keep + __shfl_xor_sync(kFull, send, m);
+        }
+    }
+    return v[0];
+}
+
+// One 32-token stage for G query heads.  Ks/Vs: [32][D] in shared memory.
+template <int D, int G, typename T, bool FULL_STAGE>
+__device__ __forceinline__ void consume_stage(const T *Ks, const T *Vs, int nvalid, int r, int c,
+                                              const float (&qf)[G][8], float (&m)[G], float (&lsum)[G],
+                                              float (&acc)[G][8]) {
+    using Gm = Geometry<D>;
+    constexpr int NI = Gm::NI, RPI = Gm::RPI, LPR = Gm::LPR;
+    float part[G][NI];
+#pragma unroll
+    for (int i = 0; i < NI; i++) {
+        const int row = i * RPI + r;
+        const uint4 raw = *reinterpret_cast<const uint4 *>(Ks + row * D + c * 8);
+        float kf[8];
+        F16Traits<T>::to_f32(raw, kf);
+#pragma unroll
+        for (int h = 0; h < G; h++) {
+            float a = qf[h][0] * kf[0];
+#pragma unroll
+            for (int e = 1; e < 8; e++) a = fmaf(qf[h][e], kf[e], a);
+            part[h][i] = a;
+        }
+    }
+    // lane (r, c) now owns token c * RPI + r of the stage
+    const int myrow = c * RPI + r;
+    float p[G];
+#pragma unroll
+    for (int h = 0; h < G; h++) {
+        float sc = reduce_scatter<NI>(part[h], c);
+        if (!FULL_STAGE && myrow >= nvalid) sc = -INFINITY;
+        const float mnew = fmaxf(m[h], warp_max(sc));
+        const float alpha = exp2f(m[h] - mnew);
+        p[h] = exp2f(sc - mnew);
+        lsum[h] = lsum[h] * alpha + p[h];
+#pragma unroll
+        for (int e = 0; e < 8; e++) acc[h][e] *= alpha;
+        m[h] = mnew;
+    }
+#pragma unroll
+    for (int i = 0; i < NI; i++) {
+        const int row = i * RPI + r;
+        const uint4 raw = *reinterpret_cast<const uint4 *>(Vs + row * D + c * 8);
+        float vf[8];
+        F16Traits<T>::to_f32(raw, vf);
+        if (!FULL_STAGE && row >= nvalid) {
+#pragma unroll
+            for (int e = 0; e < 8; e++) vf[e] = 0.f;      // rows past the context may hold anything
+        }
+#pragma unroll
+        for (int h = 0; h < G; h++) {
+            const float w = __shfl_sync(kFull, p[h], r * LPR + i);
+#pragma unroll
+            for (int e = 0; e < 8; e++) acc[h][e] = fmaf(w, vf[e], acc[h][e]);
+        }
+    }
+}
+
+struct AttnArgs {
+    void *out;                   // [S][H][D] T
+    float *ws_m;                 // [S][H][MP]
+    float *ws_l;                 // [S][H][MP]
+    float *ws_o;                 // [S][H][MP][D]
+    const void *q;               // [S][H][D]
+    const void *k_cache;         // [NB][Hkv][B][D]
+    const void *v_cache;
+    const int32_t *tables;       // [S][max_blocks]
+    const int32_t *ctx_lens;     // [S]
+    DeviceStatus *st;
+    int max_blocks;
+    int max_ctx;
+    int log2_block;
+    int num_blocks;
+    int num_heads;
+    int num_kv_heads;
+    int head_tiles;              // (H / Hkv) / G
+    int partition;               // P
+    int max_parts;               // MP
+    float scale_log2;            // scale * log2(e)
+};
+
+template <int D, int G, typename T>
+__global__ void __launch_bounds__(kThreads, 2) paged_attention_kernel(const AttnArgs a) {
+    using Gm = Geometry<D>;
+    constexpr int NSTAGE = Gm::NSTAGE, SE = Gm::STAGE_ELEMS, LPR = Gm::LPR;
+    extern __shared__ __align__(128) unsigned char smem[];
+    T *ring = reinterpret_cast<T *>(smem);                         // [NSTAGE][2][32][D]
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)NSTAGE * 2 * SE * sizeof(T));
+    uint64_t *empty = full + NSTAGE;
+    int *nvalid_s = reinterpret_cast<int *>(empty + NSTAGE);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int s = blockIdx.y, part = blockIdx.z;
+    const int g = blockIdx.x / a.head_tiles;
+    const int h0 = g * (a.head_tiles * G) + (blockIdx.x % a.head_tiles) * G;
+    const int B = 1 << a.log2_block;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NSTAGE; i++) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        fence_mbar_init();
+    }
+    __shared__ int abort_cta;
+    pdl_trigger();
+    pdl_wait();
+    if (threadIdx.x == 0) abort_cta = timed_out(a.st);
+    __syncthreads();
+    if (abort_cta) return;                                       // an earlier wait gave up
+
+    int ctx = a.ctx_lens[s];
+    if (ctx < 0 || ctx > a.max_ctx) {
+        if (threadIdx.x == 0 && blockIdx.x == 0 && part == 0) latch(a.st, kFlagBadContext, ctx);
+        ctx = ctx < 0 ? 0 : a.max_ctx;
+    }
+    const int nparts = (ctx + a.partition - 1) / a.partition;
+    if (part >= (nparts > 1 ? nparts : 1)) return;                // uniform over the CTA
+    const int tok0 = part * a.partition;
+    const int ntok = ctx - tok0 < a.partition ? ctx - tok0 : a.partition;
+    const int nstages = ntok > 0 ? (ntok + kStageRows - 1) / kStageRows : 0;
+
+    if (warp == kConsumerWarps) {
+        // ---------------- producer: block table -> bulk copies ----------------
+        const T *kc = static_cast<const T *>(a.k_cache);
+        const T *vc = static_cast<const T *>(a.v_cache);
+        const int32_t *trow = a.tables + (size_t)s * a.max_blocks;
+        const int nblk = (ctx + B - 1) >> a.log2_block;
+        const int cps = B >= kStageRows ? 1 : kStageRows >> a.log2_block;   // copies per stage
+        const int rows_per_copy = B >= kStageRows ? kStageRows : B;
+        const uint32_t copy_bytes = (uint32_t)(rows_per_copy * D * sizeof(T));
+        const uint64_t policy = policy_evict_first();
+        int win = -(1 << 30), ent = -1;
+        bool dead = false;
+        for (int k = 0; k < nstages; k++) {
+            const int t_first = tok0 + k * kStageRows;
+            const int lb0 = t_first >> a.log2_block;
+            const int off0 = t_first & (B - 1);                      // non-zero only when B > 32
+            if (lb0 < win || lb0 + cps > win + 32) {
+                win = lb0;
+                const int j = win + lane;
+                ent = j < nblk ? __ldg(trow + j) : -1;
+            }
+            int e[8];
+#pragma unroll
+            for (int j = 0; j < 8; j++) e[j] = __shfl_sync(kFull, ent, (lb0 + j - win) & 31);
+            if (lane == 0) {
+                const int slot = k % NSTAGE;
+                if (k >= NSTAGE && !dead &&
+                    !mbar_wait(&empty[slot], ((k / NSTAGE) - 1) & 1, kWaitLimitCycles)) {
+                    latch(a.st, kFlagTimeout, k);
+                    dead = true;
+                }
+                int nv = ntok - k * kStageRows < kStageRows ? ntok - k * kStageRows : kStageRows;
+                int ncopies = 0;
+                if (dead) {
+                    nv = 0;
+                } else {
+                    for (int j = 0; j < cps && j < 8; j++) {
+                        if (j * rows_per_copy >= nv) break;
+                        const int p = e[j];
+                        if (p < 0 || p >= a.num_blocks) {
+                            latch(a.st, kFlagBadBlock, p);
+                            nv = j * rows_per_copy;                  // stop the stage at the bad block
+                            break;
+                        }
+                        ncopies = j + 1;
+                    }
+                }
+                nvalid_s[slot] = nv;
+                mbar_arrive_expect_tx(&full[slot], 2u * copy_bytes * (uint32_t)ncopies);
+                for (int j = 0; j < ncopies; j++) {
+                    const size_t goff = (((size_t)e[j] * a.num_kv_heads + g) * B + off0) * D;
+                    T *dk = ring + (size_t)(slot * 2) * SE + (size_t)j * rows_per_copy * D;
+                    bulk_g2s_hint(dk, kc + goff, copy_bytes, &full[slot], policy);
+                    bulk_g2s_hint(dk + SE, vc + goff, copy_bytes, &full[slot], policy);
+                }
+            }
+            __syncwarp();
+        }
+        return;
+    }
+
+    // ---------------- consumers ----------------
+    const int r = lane / LPR, c = lane % LPR;
+    float qf[G][8];
+    {
+        const T *qp = static_cast<const T *>(a.q) + ((size_t)s * a.num_heads + h0) * D + c * 8;
+#pragma unroll
+        for (int h = 0; h < G; h++) {
+            const uint4 raw = *reinterpret_cast<const uint4 *>(qp + (size_t)h * D);
+            F16Traits<T>::to_f32(raw, qf[h]);
+#pragma unroll
+            for (int e = 0; e < 8; e++) qf[h][e] *= a.scale_log2;
+        }
+    }
+    float m[G], lsum[G], acc[G][8];
+#pragma unroll
+    for (int h = 0; h < G; h++) {
+        m[h] = -INFINITY;
+        lsum[h] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; e++) acc[h][e] = 0.f;
+    }
+    bool dead = false;
+    for (int k = warp; k < nstages; k += kConsumerWarps) {
+        const int slot = k % NSTAGE;
+        // warp-uniform, so that a give-up never splits the warp
+        const bool ok = __all_sync(kFull, mbar_wait(&full[slot], (k / NSTAGE) & 1,
+                                                    dead ? kDrainLimitCycles : kWaitLimitCycles));
+        if (!ok && !dead) {
+            if (lane == 0) latch(a.st, kFlagTimeout, k);
+            dead = true;
+        }
+        if (!dead) {
+            const int nv = nvalid_s[slot];
+            const T *Ks = ring + (size_t)(slot * 2) * SE;
+            if (nv == kStageRows)
+                consume_stage<D, G, T, true>(Ks, Ks + SE, nv, r, c, qf, m, lsum, acc);
+            else if (nv > 0)
+                consume_stage<D, G, T, false>(Ks, Ks + SE, nv, r, c, qf, m, lsum, acc);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+    }
+
+    // ---------------- merge the consumer warps ----------------
+#pragma unroll
+    for (int h = 0; h < G; h++) {
+        lsum[h] = warp_sum(lsum[h]);
+#pragma unroll
+        for (int e = 0; e < 8; e++) {
+#pragma unroll
+            for (int o = LPR; o < 32; o <<= 1) acc[h][e] += __shfl_xor_sync(kFull, acc[h][e], o);
+        }
+    }
+    named_bar_sync(1, kConsumerWarps * 32);        // every stage consumed: the ring is free
+    float *mw = reinterpret_cast<float *>(smem);   // [W][G]
+    float *lw = mw + kConsumerWarps * G;           // [W][G]
+    float *ow = lw + kConsumerWarps * G;           // [W][G][D]
+    if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < G; h++) {
+            mw[warp * G + h] = m[h];
+            lw[warp * G + h] = lsum[h];
+        }
+    }
+    if (r == 0) {
+#pragma unroll
+        for (int h = 0; h < G; h++)
+#pragma unroll
+            for (int e = 0; e < 8; e++) ow[(warp * G + h) * D + c * 8 + e] = acc[h][e];
+    }
+    named_bar_sync(1, kConsumerWarps * 32);
+    for (int idx = threadIdx.x; idx < G * D; idx += kConsumerWarps * 32) {
+        const int h = idx / D, e = idx % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; w++) M = fmaxf(M, mw[w * G + h]);
+        float L = 0.f, O = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; w++) {
+            const float mwv = mw[w * G + h];
+            const float wt = mwv == -INFINITY ? 0.f : exp2f(mwv - M);
+            L = fmaf(lw[w * G + h], wt, L);
+            O = fmaf(ow[(w * G + h) * D + e], wt, O);
+        }
+        const size_t sh = (size_t)s * a.num_heads + h0 + h;
+        if (nparts <= 1) {
+            static_cast<T *>(a.out)[sh * D + e] = F16Traits<T>::from_f32(L > 0.f ? O / L : 0.f);
+        } else {
+            const size_t sp = sh * a.max_parts + part;
+            a.ws_o[sp * D + e] = O;
+            if (e == 0) {
+                a.ws_m[sp] = M;
+                a.ws_l[sp] = L;
+            }
+        }
+    }
+}
+
+// Merge the partitions of each (sequence, head) with more than one:
+// M = max_p m_p, L = sum_p l_p 2^(m_p - M), out = sum_p o_p 2^(m_p - M) / L.
+template <int D, typename T>
+__global__ void __launch_bounds__(D) partition_reduce_kernel(const AttnArgs a) {
+    pdl_trigger();
+    pdl_wait();
+    const int h = blockIdx.x, s = blockIdx.y, e = threadIdx.x;
+    int ctx = a.ctx_lens[s];
+    ctx = ctx < 0 ? 0 : (ctx > a.max_ctx ? a.max_ctx : ctx);
+    const int np = (ctx + a.partition - 1) / a.partition;
+    if (np <= 1) return;
+    const size_t base = ((size_t)s * a.num_heads + h) * a.max_parts;
+    const float *m = a.ws_m + base;
+    const float *l = a.ws_l + base;
+    const float *o = a.ws_o + base * D;
+    float M = -INFINITY;
+    for (int p = 0; p < np; p++) M = fmaxf(M, m[p]);
+    float L = 0.f, O = 0.f;
+    for (int p = 0; p < np; p++) {
+        const float wt = exp2f(m[p] - M);
+        L = fmaf(l[p], wt, L);
+        O = fmaf(o[(size_t)p * D + e], wt, O);
+    }
+    static_cast<T *>(a.out)[((size_t)s * a.num_heads + h) * D + e] = F16Traits<T>::from_f32(L > 0.f ? O / L : 0.f);
+}
+
+constexpr int kDefaultPartition = 512;
+
+int choose_partition(int partition_size) { return partition_size > 0 ? partition_size : kDefaultPartition; }
+
+int parts_for(int max_ctx, int P) { return max_ctx > 0 ? (max_ctx + P - 1) / P : 1; }
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct WsLayout {
+    size_t m_off, l_off, o_off, bytes;
+};
+
+WsLayout ws_layout(int S, int H, int D, int MP) {
+    WsLayout w{};
+    if (MP <= 1) return w;
+    const size_t n = (size_t)S * H * MP;
+    w.m_off = 0;
+    w.l_off = align256(n * sizeof(float));
+    w.o_off = w.l_off + align256(n * sizeof(float));
+    w.bytes = w.o_off + align256(n * D * sizeof(float));
+    return w;
+}
+
+template <int D, int G, typename T> cudaError_t launch_attention(const AttnArgs &a, dim3 grid, cudaStream_t st) {
+    static bool configured = false;      // per template instance; harmless if repeated
+    auto kern = paged_attention_kernel<D, G, T>;
+    const size_t smem = smem_bytes<D, T>();
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    return launch(kern, grid, dim3(kThreads), smem, st, a);
+}
+
+template <int D, typename T> cudaError_t dispatch_g(int G, const AttnArgs &a, dim3 grid, cudaStream_t st) {
+    switch (G) {
+    case 4: return launch_attention<D, 4, T>(a, grid, st);
+    case 2: return launch_attention<D, 2, T>(a, grid, st);
+    default: return launch_attention<D, 1, T>(a, grid, st);
+    }
+}
+
+template <typename T> cudaError_t dispatch_d(int D, int G, const AttnArgs &a, dim3 grid, cudaStream_t st) {
+    return D == 64 ? dispatch_g<64, T>(G, a, grid, st) : dispatch_g<128, T>(G, a, grid, st);
+}
+
+template <typename T> cudaError_t launch_reduce(int D, const AttnArgs &a, dim3 grid, cudaStream_t st) {
+    if (D == 64) return launch(partition_reduce_kernel<64, T>, grid, dim3(64), 0, st, a);
+    return launch(partition_reduce_kernel<128, T>, grid, dim3(128), 0, st, a);
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" {
+
+int paged_attention_partition_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                   int max_context_len, int partition_size) {
+    (void)num_seqs;
+    (void)num_heads;
+    (void)num_kv_heads;
+    (void)head_dim;
+    (void)max_context_len;
+    return pkv::choose_partition(partition_size);
+}
+
+size_t paged_attention_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                      int max_context_len, int partition_size) {
+    if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_context_len <= 0 || partition_size < 0)
+        return 0;
+    const int P = paged_attention_partition_size(num_seqs, num_heads, num_kv_heads, head_dim, max_context_len,
+                                                 partition_size);
+    return pkv::ws_layout(num_seqs, num_heads, head_dim, pkv::parts_for(max_context_len, P)).bytes;
+}
+
+pkv_status paged_attention_decode(void *out, const void *query, const void *key_cache, const void *value_cache,
+                                  const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                                  int max_blocks_per_seq, int max_context_len, int block_size, int num_blocks,
+                                  int num_heads, int num_kv_heads, int head_dim, float scale, int partition_size,
+                                  void *workspace, size_t workspace_bytes, pkv_dtype dtype,
+                                  struct CUstream_st *stream) {
+    using namespace pkv;
+    if (dtype != PKV_F16 && dtype != PKV_BF16) return fail(PKV_EINVAL, "paged_attention_decode: bad dtype %d", (int)dtype);
+    if (num_seqs < 0 || num_seqs > 65535 || max_blocks_per_seq < 0 || num_blocks < 0)
+        return fail(PKV_EINVAL, "paged_attention_decode: bad sizes (seqs %d, table width %d, blocks %d)", num_seqs,
+                    max_blocks_per_seq, num_blocks);
+    if (head_dim != 64 && head_dim != 128)
+        return fail(PKV_EINVAL, "paged_attention_decode: head_dim %d not supported (64 or 128)", head_dim);
+    if (!is_pow2(block_size) || block_size < 4 || block_size > 128)
+        return fail(PKV_EINVAL, "paged_attention_decode: block_size %d not a power of two in [4, 128]", block_size);
+    if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads)
+        return fail(PKV_EINVAL, "paged_attention_decode: %d query heads do not group over %d kv heads", num_heads,
+                    num_kv_heads);
+    if (partition_size < 0 || partition_size % kStageRows)
+        return fail(PKV_EINVAL, "paged_attention_decode: partition_size %d not a multiple of %d", partition_size,
+                    kStageRows);
+    const int64_t table_cap = (int64_t)max_blocks_per_seq * block_size;
+    if (max_context_len < 0 || max_context_len > table_cap)
+        return fail(PKV_EINVAL, "paged_attention_decode: max_context_len %d beyond the table (%lld tokens)",
+                    max_context_len, (long long)table_cap);
+    if (num_seqs == 0) return PKV_OK;
+    const int max_ctx = max_context_len > 0 ? max_context_len : (int)(table_cap > INT32_MAX ? INT32_MAX : table_cap);
+    if (!out || !query || !key_cache || !value_cache || !block_tables || !context_lens)
+        return fail(PKV_EINVAL, "paged_attention_decode: NULL pointer");
+    if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) || !aligned16(value_cache))
+        return fail(PKV_EINVAL, "paged_attention_decode: pointers must be 16-byte aligned");
+    const int P = choose_partition(partition_size);
+    const int MP = parts_for(max_ctx, P);
+    if (MP > 65535) return fail(PKV_EINVAL, "paged_attention_decode: %d partitions per sequence", MP);
+    const WsLayout wl = ws_layout(num_seqs, num_heads, head_dim, MP);
+    if (wl.bytes > 0 && (!workspace || workspace_bytes < wl.bytes || !aligned16(workspace)))
+        return fail(PKV_EINVAL, "paged_attention_decode: workspace of %zu bytes needed, %zu given", wl.bytes,
+                    workspace ? workspace_bytes : (size_t)0);
+    DeviceStatus *st = status_ptr();
+    if (!st) return fail(PKV_ECUDA, "paged_attention_decode: no device status word");
+
+    const int group = num_heads / num_kv_heads;
+    const int G = group % 4 == 0 ? 4 : (group % 2 == 0 ? 2 : 1);
+    AttnArgs a;
+    a.out = out;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    a.ws_m = wl.bytes ? reinterpret_cast<float *>(ws + wl.m_off) : nullptr;
+    a.ws_l = wl.bytes ? reinterpret_cast<float *>(ws + wl.l_off) : nullptr;
+    a.ws_o = wl.bytes ? reinterpret_cast<float *>(ws + wl.o_off) : nullptr;
+    a.q = query;
+    a.k_cache = key_cache;
+    a.v_cache = value_cache;
+    a.tables = block_tables;
+    a.ctx_lens = context_lens;
+    a.st = st;
+    a.max_blocks = max_blocks_per_seq;
+    a.max_ctx = max_ctx;
+    a.log2_block = ilog2(block_size);
+    a.num_blocks = num_blocks;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_tiles = group / G;
+    a.partition = P;
+    a.max_parts = MP;
+    a.scale_log2 = scale * kLog2e;
+
+    const dim3 grid((unsigned)(num_kv_heads * a.head_tiles), (unsigned)num_seqs, (unsigned)MP);
+    cudaError_t e = dtype == PKV_F16 ? dispatch_d<__half>(head_dim, G, a, grid, stream)
+                                     : dispatch_d<__nv_bfloat16>(head_dim, G, a, grid, stream);
+    if (e != cudaSuccess) return fail(PKV_ECUDA, "paged_attention_decode: launch: %s", cudaGetErrorString(e));
+    if (MP > 1) {
+        const dim3 rgrid((unsigned)num_heads, (unsigned)num_seqs);
+        e = dtype == PKV_F16 ? launch_reduce<__half>(head_dim, a, rgrid, stream)
+                             : launch_reduce<__nv_bfloat16>(head_dim, a, rgrid, stream);
+        if (e != cudaSuccess) return fail(PKV_ECUDA, "paged_attention_decode: reduce launch: %s", cudaGetErrorString(e));
+    }
+    return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,179 @@
+// Device-side helpers for the sm_103a kernels: the latched status word,
+// programmatic dependent launch, mbarriers with bounded waits, 1-D bulk
+// (TMA) copies into shared memory, and 16-bit <-> fp32 conversion.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace pkv {
+
+// ---- per-device status word ---------------------------------------------
+
+struct DeviceStatus {
+    unsigned int flags;        // kFlag* bits; sticky until pkv_check clears them
+    unsigned int have_first;   // 1 once first_bad/first_flag hold a value
+    long long first_bad;       // the first offending value (slot, block id, ...)
+    unsigned int first_flag;
+    unsigned int pad;
+};
+
+enum : unsigned int {
+    kFlagBadSlot = 1u,         // slot outside the pool
+    kFlagBadBlock = 2u,        // block-table entry outside the pool
+    kFlagBadPair = 4u,         // copy pair with a block id outside the pool
+    kFlagTimeout = 8u,         // a bounded wait gave up
+    kFlagBadContext = 16u,     // context length negative or beyond the table
+};
+
+__device__ __forceinline__ void latch(DeviceStatus *st, unsigned int flag, long long value) {
+    atomicOr(&st->flags, flag);
+    if (atomicCAS(&st->have_first, 0u, 1u) == 0u) {
+        st->first_bad = value;
+        st->first_flag = flag;
+    }
+}
+
+// Cycles a wait on an mbarrier may take before the kernel gives up (about
+// 0.14 s at 1.9 GHz; a stage normally lands within microseconds).
+constexpr long long kWaitLimitCycles = 1ll << 28;
+// After one wait has given up: how long to wait for copies still in flight.
+constexpr long long kDrainLimitCycles = 1ll << 25;
+
+// True once any kernel has latched a timeout that pkv_check has not yet
+// cleared; kernels then return at once instead of waiting again.
+__device__ __forceinline__ bool timed_out(const DeviceStatus *st) {
+    return (*reinterpret_cast<const volatile unsigned int *>(&st->flags) & kFlagTimeout) != 0;
+}
+
+// ---- programmatic dependent launch ---------------------------------------
+
+// Blocks until the grids this one depends on have completed and their
+// memory is visible; a no-op for a launch without the PDL attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next grid in the stream start launching.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---- mbarrier --------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// Makes initialised barriers visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile(
+        "{\n\t.reg .b64 st;\n\t"
+        "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+        "r"(bytes)
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile(
+        "{\n\t.reg .b64 st;\n\t"
+        "mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Wait for the phase with the given parity to complete; false if it has not
+// within `limit` cycles.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long long limit) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (uint32_t it = 0; it < (1u << 28); ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (clock64() - t0 > limit) return false;
+    }
+    return false;
+}
+
+// ---- 1-D bulk copy (TMA, no tensor map) -----------------------------------
+
+// bytes from global to this CTA's shared memory; completion is counted on
+// `bar` as transaction bytes.  Both addresses 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_g2s(void *smem_dst, const void *gmem_src, uint32_t bytes,
+                                         uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(smem_dst)),
+        "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Same, with an L2 cache-policy hint (a createpolicy result).
+__device__ __forceinline__ void bulk_g2s_hint(void *smem_dst, const void *gmem_src, uint32_t bytes,
+                                              uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_u32(smem_dst)),
+        "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Named barrier over `count` threads (a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// ---- 16-bit element types --------------------------------------------------
+
+template <typename T> struct F16Traits;
+
+template <> struct F16Traits<__half> {
+    // Eight halves (one 16-byte vector) to fp32.
+    static __device__ __forceinline__ void to_f32(const uint4 &raw, float f[8]) {
+        const __half2 *h = reinterpret_cast<const __half2 *>(&raw);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            float2 v = __half22float2(h[i]);
+            f[2 * i] = v.x;
+            f[2 * i + 1] = v.y;
+        }
+    }
+    static __device__ __forceinline__ __half from_f32(float x) { return __float2half_rn(x); }
+};
+
+template <> struct F16Traits<__nv_bfloat16> {
+    static __device__ __forceinline__ void to_f32(const uint4 &raw, float f[8]) {
+        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            float2 v = __bfloat1622float2(h[i]);
+            f[2 * i] = v.x;
+            f[2 * i + 1] = v.y;
+        }
+    }
+    static __device__ __forceinline__ __nv_bfloat16 from_f32(float x) { return __float2bfloat16_rn(x); }
+};
+
+}  // namespace pkv

@@ -1,0 +1,130 @@
+"""A one-layer paged KV cache engine: the device K/V pools, the native block
+allocator, and the decode step that ties the three device calls together.
+
+One decode iteration ("vLLM & PagedAttention: Efficient Memory Management
+for LLM Serving", §V): allocate physical blocks for the batch's new tokens
+(copy-on-write where a sequence writes into a shared block, §VII), copy the
+shared blocks, write the new keys and values at their slots, then run the
+paged attention kernel over the block tables.  Host bookkeeping happens in
+the native allocator; the four device steps run in libpkv's kernels.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import (BlockAllocator, copy_blocks, kv_reshape_and_cache, paged_attention_decode,
+               paged_attention_workspace_size)
+
+
+@dataclasses.dataclass
+class StepPlan:
+    """Host-side result of allocating one decode step."""
+
+    seqs: np.ndarray          # int32 [n]
+    slots: np.ndarray         # int64 [n]
+    pairs: np.ndarray         # int32 [m][2] copy-on-write (src, dst)
+    tables: np.ndarray        # int32 [n][max_blocks]
+    context_lens: np.ndarray  # int32 [n]
+
+
+@dataclasses.dataclass
+class DeviceStep:
+    """The same plan on the device."""
+
+    slots: torch.Tensor
+    pairs: torch.Tensor
+    tables: torch.Tensor
+    context_lens: torch.Tensor
+    max_context_len: int
+
+
+class PagedKVCache:
+    def __init__(self, num_blocks: int, num_kv_heads: int, head_dim: int, block_size: int,
+                 dtype: torch.dtype, device, max_blocks_per_seq: int,
+                 free_order: Optional[Sequence[int]] = None,
+                 key_cache: Optional[torch.Tensor] = None, value_cache: Optional[torch.Tensor] = None):
+        shape = (num_blocks, num_kv_heads, block_size, head_dim)
+        self.device = torch.device(device)
+        self.key_cache = key_cache if key_cache is not None else torch.empty(shape, dtype=dtype, device=self.device)
+        self.value_cache = value_cache if value_cache is not None else torch.empty(shape, dtype=dtype,
+                                                                                    device=self.device)
+        assert tuple(self.key_cache.shape) == shape and tuple(self.value_cache.shape) == shape
+        self.alloc = BlockAllocator(num_blocks, block_size, free_order)
+        self.num_blocks, self.num_kv_heads, self.head_dim, self.block_size = shape[0], shape[1], shape[3], shape[2]
+        self.max_blocks_per_seq = max_blocks_per_seq
+        self._ws: Optional[torch.Tensor] = None
+
+    # -- host bookkeeping ------------------------------------------------------
+    def new_sequence(self, length: int) -> int:
+        return self.alloc.seq_new(length)
+
+    def fork(self, seq: int) -> int:
+        return self.alloc.fork(seq)
+
+    def free(self, seq: int) -> None:
+        self.alloc.free(seq)
+
+    def plan_step(self, seqs: Sequence[int]) -> StepPlan:
+        """Append one token to each sequence (all or nothing) and build the
+        tables the attention kernel reads."""
+        s = np.asarray(seqs, dtype=np.int32)
+        slots, pairs = self.alloc.append_batch(s)
+        tables, ctx = self.alloc.build_block_tables(s, self.max_blocks_per_seq)
+        return StepPlan(s, slots, pairs, tables, ctx)
+
+    def plan_tables(self, seqs: Sequence[int]) -> StepPlan:
+        """Tables of the sequences as they stand (no new token)."""
+        s = np.asarray(seqs, dtype=np.int32)
+        tables, ctx = self.alloc.build_block_tables(s, self.max_blocks_per_seq)
+        return StepPlan(s, np.empty(0, np.int64), np.empty((0, 2), np.int32), tables, ctx)
+
+    def upload(self, plan: StepPlan, non_blocking: bool = False) -> DeviceStep:
+        d = self.device
+        return DeviceStep(
+            slots=torch.from_numpy(plan.slots).to(d, non_blocking=non_blocking),
+            pairs=torch.from_numpy(np.ascontiguousarray(plan.pairs)).to(d, non_blocking=non_blocking),
+            tables=torch.from_numpy(plan.tables).to(d, non_blocking=non_blocking),
+            context_lens=torch.from_numpy(plan.context_lens).to(d, non_blocking=non_blocking),
+            max_context_len=int(plan.context_lens.max()) if plan.context_lens.size else 0)
+
+    # -- device steps ------------------------------------------------------------
+    def workspace(self, num_seqs: int, num_heads: int, max_context_len: int, partition_size: int = 0):
+        need = paged_attention_workspace_size(num_seqs, num_heads, self.num_kv_heads, self.head_dim,
+                                              max_context_len, partition_size)
+        if need == 0:
+            return None
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty(need, dtype=torch.uint8, device=self.device)
+        return self._ws
+
+    def copy_on_write(self, pairs: torch.Tensor) -> None:
+        if pairs.numel():
+            copy_blocks(self.key_cache, pairs)
+            copy_blocks(self.value_cache, pairs)
+
+    def write(self, key: torch.Tensor, value: torch.Tensor, slots: torch.Tensor) -> None:
+        kv_reshape_and_cache(key, value, self.key_cache, self.value_cache, slots)
+
+    def attend(self, query: torch.Tensor, step: DeviceStep, out: Optional[torch.Tensor] = None,
+               scale: Optional[float] = None, partition_size: int = 0,
+               max_context_len: Optional[int] = None) -> torch.Tensor:
+        if out is None:
+            out = torch.empty_like(query)
+        mcl = step.max_context_len if max_context_len is None else max_context_len
+        ws = self.workspace(query.shape[0], query.shape[1], mcl, partition_size)
+        return paged_attention_decode(out, query, self.key_cache, self.value_cache, step.tables,
+                                      step.context_lens, scale=scale, max_context_len=mcl,
+                                      partition_size=partition_size, workspace=ws)
+
+    def decode(self, query: torch.Tensor, key: torch.Tensor, value: torch.Tensor, step: DeviceStep,
+               out: Optional[torch.Tensor] = None, scale: Optional[float] = None,
+               partition_size: int = 0) -> torch.Tensor:
+        """The device half of one decode iteration: copy-on-write copies, the
+        new tokens' cache write, then attention (which reads the new tokens)."""
+        self.copy_on_write(step.pairs)
+        self.write(key, value, step.slots)
+        return self.attend(query, step, out, scale, partition_size)

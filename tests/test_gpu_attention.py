@@ -1,0 +1,221 @@
+"""paged_attention_decode against the oracle on the GPU through the C ABI:
+every workload (small sizes in full, full sizes on sampled sequences and
+heads), the split-context path, GQA groupings, block sizes, head sizes, and
+the degenerate cases."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_139_gb300 as pkv
+import workloads
+from cases import Case, assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(c: Case, heads=None, what=""):
+    c.check_allocator()
+    want = c.oracle_out(heads)
+    got = c.gpu_out()
+    if heads is not None:
+        rows = tuple(np.array(heads).T)
+        got, want = got[rows], want[rows]
+    return assert_close(got, want, what)
+
+
+def _custom(name="custom", S=3, H=4, Hkv=2, d=128, B=16, dtype="f16", ctx=(1, 40, 333), max_ctx=None,
+            seed=77, partition=0):
+    ctx = np.asarray(ctx, np.int64)
+    mc = int(max_ctx or max(int(ctx.max()), 1))
+    mb = -(-mc // B)
+    nb = int(sum(-(-int(c) // B) for c in ctx)) + 5
+    return workloads.Workload(name, S, H, Hkv, d, B, dtype, ctx, mb, nb, seed, partition)
+
+
+def test_tiny_workload(cuda_device):
+    c = Case(workloads.tiny(), cuda_device)
+    _check(c, what="tiny")
+    k, v = c.gpu_cache_blocks()
+    ok, ov = c.oracle_caches()
+    assert np.array_equal(k, ok) and np.array_equal(v, ov)
+
+
+def test_opt13b_small(cuda_device):
+    _check(Case(workloads.opt13b(num_seqs=8), cuda_device), what="opt13b x8")
+
+
+def test_opt13b_full(cuda_device):
+    """The 64-sequence OPT-13B layer batch in full, in the default launch."""
+    _check(Case(workloads.opt13b(), cuda_device), what="opt13b")
+
+
+@pytest.mark.parametrize("B", [8, 16, 32])
+def test_llama7b_small(cuda_device, B):
+    _check(Case(workloads.llama7b(block_size=B, num_seqs=12, max_ctx=1500), cuda_device), what=f"llama7b B={B}")
+
+
+@pytest.mark.parametrize("B", [8, 16, 32])
+def test_llama7b_full_sampled(cuda_device, B):
+    """The full 256 x uniform[1,4096] batch: all heads of 6 sampled sequences."""
+    w = workloads.llama7b(block_size=B)
+    sel = [0, 17, 99, 128, 201, 255]
+    c = Case(w, cuda_device, gen_device="cuda", subset=sel)
+    _check(c, what=f"llama7b full B={B}")
+
+
+def test_sampling_small(cuda_device):
+    _check(Case(workloads.sampling(num_prompts=6, max_suffix=60), cuda_device), what="sampling x6")
+
+
+def test_sampling_full_sampled(cuda_device):
+    c = Case(workloads.sampling(), cuda_device, subset=[0, 1, 2, 3, 101, 202, 255])
+    _check(c, what="sampling full")
+
+
+def test_longgqa_small(cuda_device):
+    _check(Case(workloads.longgqa(num_seqs=2, ctx_len=4096), cuda_device), what="longgqa small")
+
+
+def test_longgqa_full_sampled(cuda_device):
+    """8 x 32768 tokens, bf16, GQA 32/8, partitions of 512: sampled heads of
+    two sequences (the oracle computes them one by one)."""
+    w = workloads.longgqa()
+    c = Case(w, cuda_device, gen_device="cuda", subset=[0, 7])
+    heads = [(0, 0), (0, 3), (0, 17), (1, 30), (1, 31), (1, 4)]
+    _check(c, heads=heads, what="longgqa full")
+
+
+@pytest.mark.parametrize("H,Hkv", [(4, 4), (4, 2), (8, 2), (12, 4), (16, 2), (10, 2), (6, 6), (7, 1)])
+def test_head_groupings(cuda_device, H, Hkv):
+    w = _custom(H=H, Hkv=Hkv, ctx=(1, 17, 200, 513, 1030), S=5, dtype="bf16")
+    c = Case(w, cuda_device, partition_size=256)
+    _check(c, what=f"H={H} Hkv={Hkv}")
+
+
+@pytest.mark.parametrize("B", [4, 8, 16, 32, 64, 128])
+@pytest.mark.parametrize("d", [64, 128])
+def test_block_and_head_sizes(cuda_device, B, d):
+    w = _custom(d=d, B=B, ctx=(1, 3, 31, 32, 33, 64, 127, 500, 1027), S=9, dtype="f16" if B % 8 else "bf16")
+    for P in (0, 32, 128):
+        c = Case(w, cuda_device, partition_size=P)
+        _check(c, what=f"B={B} d={d} P={P}")
+
+
+@pytest.mark.parametrize("P", [32, 64, 96, 512, 4096])
+def test_partition_sizes_agree(cuda_device, P):
+    """Split and unsplit runs of the same batch both match the oracle."""
+    w = _custom(H=8, Hkv=2, ctx=(5, 511, 512, 513, 2048, 3001), S=6, max_ctx=4096)
+    c = Case(w, cuda_device, partition_size=P)
+    _check(c, what=f"P={P}")
+
+
+def test_context_zero_and_one(cuda_device):
+    w = _custom(ctx=(1, 2, 1, 40), S=4)
+    c = Case(w, cuda_device)
+    _check(c, what="short")
+    # ctx = 1 returns the single value exactly up to output rounding
+    v = c.eng.value_cache[int(c.plan.tables[0, 0]), 0, 0].double().cpu().numpy()
+    assert np.array_equal(c.gpu_out()[0, 0], v)
+    # ctx = 0: zeros
+    ctx0 = torch.zeros_like(c.dev.context_lens)
+    step = dataclasses.replace(c.dev, context_lens=ctx0)
+    out = c.eng.attend(c.q_dev, step, max_context_len=64)
+    pkv.check()
+    assert int(out.abs().sum().item()) == 0
+
+
+def test_permutation_invariance_bit_exact(cuda_device):
+    """Moving the blocks to other physical ids changes no output bit."""
+    w = _custom(H=8, Hkv=2, ctx=(100, 700, 1500), S=3, dtype="bf16")
+    c = Case(w, cuda_device, partition_size=256)
+    out1 = c.out.clone()
+    perm = torch.randperm(w.num_blocks, generator=torch.Generator().manual_seed(5)).to(cuda_device)
+    kc2 = torch.empty_like(c.eng.key_cache)
+    vc2 = torch.empty_like(c.eng.value_cache)
+    kc2[perm] = c.eng.key_cache
+    vc2[perm] = c.eng.value_cache
+    t = c.dev.tables.long()
+    t2 = torch.where(t >= 0, perm[t.clamp(min=0)], t).to(torch.int32)
+    out2 = torch.empty_like(out1)
+    pkv.paged_attention_decode(out2, c.q_dev, kc2, vc2, t2, c.dev.context_lens, partition_size=256)
+    pkv.check()
+    assert torch.equal(out1, out2)
+
+
+def test_identity_table_equals_contiguous_oracle(cuda_device):
+    """With the identity table (each sequence's blocks adjacent) the kernel
+    equals the oracle, which here is plain contiguous attention."""
+    S, H, d, B, mb = 4, 4, 128, 16, 40
+    q = workloads.normal((S, H, d), "f16", 1).to(cuda_device)
+    kc = workloads.normal((S * mb, H, B, d), "f16", 2).to(cuda_device)
+    vc = workloads.normal((S * mb, H, B, d), "f16", 3).to(cuda_device)
+    tables = torch.arange(S * mb, dtype=torch.int32, device=cuda_device).view(S, mb)
+    ctx = torch.tensor([640, 1, 77, 500], dtype=torch.int32, device=cuda_device)
+    out = torch.empty_like(q)
+    pkv.paged_attention_decode(out, q, kc, vc, tables, ctx)
+    pkv.check()
+    want = oracle.paged_attention(q.cpu(), kc.cpu(), vc.cpu(), tables.cpu().numpy(), ctx.cpu().numpy(), "f16")
+    assert_close(out.double().cpu().numpy(), want, "identity table")
+
+
+def test_bad_block_id_latches_eindex(cuda_device):
+    w = _custom(ctx=(50, 90), S=2)
+    c = Case(w, cuda_device)
+    pkv.check()
+    t = c.dev.tables.clone()
+    t[1, 2] = w.num_blocks + 3
+    pkv.paged_attention_decode(torch.empty_like(c.q_dev), c.q_dev, c.eng.key_cache, c.eng.value_cache, t,
+                               c.dev.context_lens)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.check()
+    assert e.value.status_name == "PKV_EINDEX" and "block" in str(e.value)
+    pkv.check()                                          # cleared
+
+
+def test_context_beyond_bound_latches_eindex(cuda_device):
+    w = _custom(ctx=(50, 90), S=2)
+    c = Case(w, cuda_device)
+    pkv.paged_attention_decode(torch.empty_like(c.q_dev), c.q_dev, c.eng.key_cache, c.eng.value_cache,
+                               c.dev.tables, c.dev.context_lens, max_context_len=64)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.check()
+    assert e.value.status_name == "PKV_EINDEX" and "context" in str(e.value)
+
+
+def test_bounded_wait_times_out_and_context_survives(cuda_device):
+    L = pkv._lib.load()
+    import ctypes
+    s = torch.cuda.current_stream()
+    assert L.pkv_selftest_wait_timeout(1 << 20, ctypes.c_void_p(s.cuda_stream)) == 0
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.check()
+    assert e.value.status_name == "PKV_ETIMEOUT"
+    # the context is still usable
+    test_tiny_workload(cuda_device)
+
+
+def test_output_guard_bytes(cuda_device):
+    """Nothing outside out[S][H][d] is written."""
+    w = _custom(H=8, Hkv=2, ctx=(33, 1000), S=2)
+    c = Case(w, cuda_device, partition_size=128)
+    n = c.q_dev.numel()
+    buf = torch.full((n + 2048,), 7.0, dtype=c.q_dev.dtype, device=cuda_device)
+    out = buf[1024:1024 + n].view_as(c.q_dev)
+    c.rerun_attention(out=out)
+    pkv.check()
+    assert bool((buf[:1024] == 7).all()) and bool((buf[1024 + n:] == 7).all())
+    assert torch.equal(out, c.out)
+
+
+def test_launch_count_and_native_library(cuda_device):
+    before = pkv.launch_count()
+    c = Case(_custom(ctx=(600, 700), S=2, H=4, Hkv=4), cuda_device, partition_size=256)
+    pkv.check()
+    # cache write + attention + partition merge
+    assert pkv.launch_count() - before == 3
+    import os
+    maps = open("/proc/self/maps").read()
+    assert os.path.realpath(pkv.library_path()) in maps
