@@ -44,9 +44,17 @@ template <int D> struct Geometry {
     static constexpr int LPR = D / 8;       // lanes per row (16 bytes each)
     static constexpr int RPI = 32 / LPR;    // rows covered by one warp-wide load
     static constexpr int NI = kStageRows / RPI;   // loads per stage (== LPR)
-    static constexpr int NSTAGE = D >= 128 ? 6 : 8;
+    // Stage k goes to consumer warp k % W and ring slot k % NSTAGE.  NSTAGE is
+    // a multiple of W, so every slot belongs to one warp, which waits for its
+    // phases in order: a parity wait can never see a phase two ahead.
+    static constexpr int SLOTS_PER_WARP = D >= 128 ? 1 : 2;
+    static constexpr int NSTAGE = kConsumerWarps * SLOTS_PER_WARP;
     static constexpr int STAGE_ELEMS = kStageRows * D;   // per tensor
+    static_assert(NSTAGE % kConsumerWarps == 0, "ring slots must divide among the consumer warps");
 };
+
+// CTAs per SM the register budget is sized for (shared memory allows 3).
+template <int G> constexpr int min_ctas() { return G >= 4 ? 2 : 3; }
 
 template <int D, typename T> constexpr size_t smem_bytes() {
     using Gm = Geometry<D>;
@@ -162,7 +170,7 @@ struct AttnArgs {
 };
 
 template <int D, int G, typename T>
-__global__ void __launch_bounds__(kThreads, 2) paged_attention_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(kThreads, min_ctas<G>()) paged_attention_kernel(const AttnArgs a) {
     using Gm = Geometry<D>;
     constexpr int NSTAGE = Gm::NSTAGE, SE = Gm::STAGE_ELEMS, LPR = Gm::LPR;
     extern __shared__ __align__(128) unsigned char smem[];

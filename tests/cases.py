@@ -16,6 +16,7 @@ import numpy as np
 import torch
 
 import oracle
+import paged_kv_cache_139_gb300 as pkv
 import workloads
 from paged_kv_cache_139_gb300.engine import PagedKVCache
 
@@ -142,10 +143,13 @@ class Case:
         self.k_dev, self.v_dev = self.key.to(d), self.value.to(d)
         self.out = eng.decode(self.q_dev, self.k_dev, self.v_dev, self.dev, partition_size=self.partition_size)
         self.eng = eng
+        pkv.check()                     # raises (and clears) any error the device latched
 
     def rerun_attention(self, partition_size=None, out=None):
         ps = self.partition_size if partition_size is None else partition_size
-        return self.eng.attend(self.q_dev, self.dev, out=out, partition_size=ps)
+        o = self.eng.attend(self.q_dev, self.dev, out=out, partition_size=ps)
+        pkv.check()
+        return o
 
     # -- oracle side -----------------------------------------------------------------
     def check_allocator(self):
