@@ -81,12 +81,13 @@ def hbm_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def profile_traffic(workload_name: str):
+def profile_traffic(workload_name: str, version: int):
     """DRAM bytes per launch of the attention kernel from a committed ncu
-    summary (a line 'traffic_bytes_per_launch[<workload>]: N'), else None."""
+    summary (a line 'traffic_bytes_per_launch[<workload>@<library version>]: N'),
+    else None: a figure taken on another kernel version does not count."""
     for f in sorted((ROOT / "profiles").glob("*.md")):
         for line in f.read_text().splitlines():
-            key = f"traffic_bytes_per_launch[{workload_name}]:"
+            key = f"traffic_bytes_per_launch[{workload_name}@{version}]:"
             if line.strip().startswith(key):
                 try:
                     return float(line.split(":", 1)[1].split()[0])
@@ -207,6 +208,18 @@ def run_reference(args, rank: int, world: int):
     print(json.dumps(line))
 
 
+def aggregate(t_step_ms: float, nbytes: float, dist=None, device="cpu"):
+    """Whole-job figures over the ranks: the slowest rank's step time and the
+    sum of every rank's bytes (host control traffic only; no data moves)."""
+    if dist is None:
+        return t_step_ms, float(nbytes)
+    t = torch.tensor([t_step_ms], dtype=torch.float64, device=device)
+    b = torch.tensor([float(nbytes)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(b.item())
+
+
 # -- our arm -----------------------------------------------------------------------------
 
 def run_ours(args, rank: int, world: int):
@@ -238,10 +251,18 @@ def run_ours(args, rank: int, world: int):
     def device_step():
         eng.decode(q, key, value, step, out=out, partition_size=P)
 
-    # warm-up (also checks that the step runs clean)
-    for _ in range(args.warmup):
+    # Clocks are sampled from the start of the warm-up to the end of the e2e
+    # leg (the GPU runs the same step throughout); the warm-up runs at least W
+    # steps and at least one second so that the sampler sees the GPU under load.
+    clk = ClockSampler(dev.index).__enter__()
+    t_w = time.perf_counter()
+    n_w = 0
+    while n_w < args.warmup or time.perf_counter() - t_w < 1.0:
         flush.zero_()
         device_step()
+        n_w += 1
+        if n_w % 16 == 0:
+            torch.cuda.synchronize(dev)
     pkv.check()
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -251,18 +272,17 @@ def run_ours(args, rank: int, world: int):
         dist.barrier()
     torch.cuda.synchronize(dev)
     launches0 = pkv.launch_count()
-    with ClockSampler(dev.index) as clk:
-        wall0 = time.perf_counter()
-        for i in range(args.steps):
-            flush.zero_()                                     # L2 flushed before every step
-            starts[i].record(stream)
-            eng.copy_on_write(step.pairs)
-            eng.write(key, value, step.slots)
-            mids[i].record(stream)
-            eng.attend(q, step, out=out, partition_size=P)
-            ends[i].record(stream)
-        torch.cuda.synchronize(dev)
-        wall = time.perf_counter() - wall0
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()                                         # L2 flushed before every step
+        starts[i].record(stream)
+        eng.copy_on_write(step.pairs)
+        eng.write(key, value, step.slots)
+        mids[i].record(stream)
+        eng.attend(q, step, out=out, partition_size=P)
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
     if dist:
         dist.barrier()
     launches = pkv.launch_count() - launches0
@@ -322,22 +342,16 @@ def run_ours(args, rank: int, world: int):
                "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3}
         pkv.check()
 
-    # the slowest rank sets the time
-    t_step_max = t_step
-    total_bytes = kv_bytes
-    if dist:
-        x = torch.tensor([t_step, float(kv_bytes)], dtype=torch.float64, device=dev)
-        y = x.clone()
-        dist.all_reduce(x[:1], op=dist.ReduceOp.MAX)
-        dist.all_reduce(y[1:], op=dist.ReduceOp.SUM)
-        t_step_max, total_bytes = float(x[0]), float(y[1])
+    clk.__exit__(None, None, None)
+    t_step_max, total_bytes = aggregate(t_step, kv_bytes, dist, dev)
     if rank != 0:
         return
 
     peak, peak_src = hbm_peak()
     value = total_bytes / (t_step_max * 1e-3) / 1e9
     attn_gbs = kv_bytes / (t_attn * 1e-3) / 1e9
-    traffic = profile_traffic(args.workload if args.workload != "llama7b" else f"llama7b_B{w.block_size}")
+    traffic = profile_traffic(args.workload if args.workload != "llama7b" else f"llama7b_B{w.block_size}",
+                              pkv.version())
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_step_max, "higher_is_better": True, "scaling": "weak",
@@ -355,7 +369,7 @@ def run_ours(args, rank: int, world: int):
         "paged_overhead": {"contiguous_ms": t_contig, "paged_ms": t_attn,
                            "slowdown_pct": 100.0 * (t_attn / t_contig - 1.0)},
         "gpu_launches": launches,
-        "clocks": clk.summary(),
+        "clocks": {**clk.summary(), "window": "warm-up + timed + e2e legs"},
         "wall_s_timed_region": wall,
         "e2e": e2e,
     }
