@@ -120,6 +120,38 @@ pkv_status paged_attention_decode(void *out_dev, const void *query_dev,
                                   size_t workspace_bytes, pkv_dtype dtype,
                                   struct CUstream_st *stream);
 
+/* ---------------------------------------------------------------------------
+ * paged_attention_decode_noalloc -- paged_attention_decode for callers that
+ * cannot allocate device memory.  The pages have no counterpart: this is an
+ * interface convenience of this library.
+ *
+ * Some callers may not call cudaMalloc where they run attention: a plugin
+ * that a host framework invokes while it captures a CUDA graph or from a
+ * latency-critical execution callback (allocating there synchronises the
+ * device or is refused), or a service that fixes its device-memory budget at
+ * start-up.  This call takes no workspace: the partition partials live in a
+ * fixed 16 MiB array in the library's own device memory, which every GPU that
+ * loads the library holds until the process exits.  The caller still owns
+ * and passes every input and output; the arguments and results are those of
+ * paged_attention_decode.
+ *   - Sizes whose partials would exceed 16 MiB (see
+ *     paged_attention_workspace_size) return PKV_EINVAL, launching nothing.
+ *   - The first call on each device looks up the array's device address (no
+ *     allocation); make that first call before any stream capture.
+ *   - All calls on a device share the one array: calls that may overlap on
+ *     the GPU (other streams, other threads) race and give wrong results; one
+ *     call at a time per device.  The array needs no clearing between calls.
+ * ------------------------------------------------------------------------- */
+pkv_status paged_attention_decode_noalloc(void *out_dev, const void *query_dev,
+                                          const void *key_cache_dev, const void *value_cache_dev,
+                                          const int32_t *block_tables_dev,
+                                          const int32_t *context_lens_dev, int num_seqs,
+                                          int max_blocks_per_seq, int max_context_len,
+                                          int block_size, int num_blocks, int num_heads,
+                                          int num_kv_heads, int head_dim, float scale,
+                                          int partition_size, pkv_dtype dtype,
+                                          struct CUstream_st *stream);
+
 /* Bytes of workspace paged_attention_decode needs for these sizes (0 when no
  * context can span more than one partition).  partition_size as above. */
 size_t paged_attention_workspace_size(int num_seqs, int num_heads, int num_kv_heads,

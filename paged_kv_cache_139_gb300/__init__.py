@@ -24,7 +24,8 @@ import torch
 from ._lib import STATUS, load
 
 __all__ = ["PkvError", "PkvOOM", "kv_reshape_and_cache", "paged_attention_decode",
-           "paged_attention_workspace_size", "paged_attention_partition_size", "copy_blocks",
+           "paged_attention_decode_noalloc", "paged_attention_workspace_size",
+           "paged_attention_partition_size", "copy_blocks",
            "validate_copy_pairs", "check", "launch_count", "version", "BlockAllocator", "library_path"]
 
 PKV_F16, PKV_BF16 = 0, 1
@@ -164,6 +165,32 @@ def paged_attention_decode(out: torch.Tensor, query: torch.Tensor, key_cache: to
         S, mb, max_context_len, B, NB, H, Hkv, d, float(scale), partition_size, ws_ptr, ws_bytes,
         _dtype_code(query), _stream(stream, query.device))
     _ck(rc, "paged_attention_decode")
+    return out
+
+
+def paged_attention_decode_noalloc(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                                   value_cache: torch.Tensor, block_tables: torch.Tensor,
+                                   context_lens: torch.Tensor, scale: Optional[float] = None,
+                                   max_context_len: int = 0, partition_size: int = 0,
+                                   stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """paged_attention_decode without a workspace: for callers that may not
+    allocate device memory when they run attention.  The partition partials
+    use the library's built-in 16 MiB device array, shared by every call on a
+    device (one call at a time); larger sizes raise PkvError (PKV_EINVAL)."""
+    S, H, d = query.shape
+    NB, Hkv, B, d2 = key_cache.shape
+    if d2 != d or out.shape != query.shape or value_cache.shape != key_cache.shape:
+        raise ValueError("paged_attention_decode_noalloc: shape mismatch")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise ValueError("paged_attention_decode_noalloc: block_tables must be [S][max_blocks], context_lens [S]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    rc = load().paged_attention_decode_noalloc(
+        _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
+        _dev(block_tables, "block_tables", torch.int32), _dev(context_lens, "context_lens", torch.int32),
+        S, block_tables.shape[1], max_context_len, B, NB, H, Hkv, d, float(scale), partition_size,
+        _dtype_code(query), _stream(stream, query.device))
+    _ck(rc, "paged_attention_decode_noalloc")
     return out
 
 

@@ -20,6 +20,8 @@ SIGNATURES = {
     "kv_reshape_and_cache": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _p]),
     "paged_attention_decode": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _p,
                                     _sz, _i, _p]),
+    "paged_attention_decode_noalloc": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i,
+                                            _i, _p]),
     "paged_attention_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
     "paged_attention_partition_size": (_i, [_i, _i, _i, _i, _i, _i]),
     "copy_blocks": (_i, [_p, _p, _i, _i64, _i, _p]),
