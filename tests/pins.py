@@ -359,3 +359,25 @@ def pin_waste_example():
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
+
+
+def run_all(lib_path=None):
+    """Run every pin (against the oracle build at lib_path, if given) and
+    return the names of the pins that failed."""
+    if lib_path is not None:
+        oracle._lib = oracle.load(lib_path)
+    failed = []
+    for pin in ALL_PINS:
+        try:
+            pin()
+        except (AssertionError, ValueError):
+            failed.append(pin.__name__)
+    return failed
+
+
+if __name__ == "__main__":
+    # python tests/pins.py <liboracle.so>: used by the planted-mistake test, one
+    # process per mutant, so that a mutant that corrupts memory cannot touch the
+    # test process.
+    import sys
+    print(json.dumps(run_all(sys.argv[1] if len(sys.argv) > 1 else None)))

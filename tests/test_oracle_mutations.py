@@ -1,15 +1,19 @@
 """Plant plausible mistakes in copies of the oracle's C source and check that
 the pins catch every one (CPU only).  The oracle under test is never edited;
-each mutant is compiled to a temporary library and swapped in for the run."""
+each mutant is compiled to a temporary library and run in a process of its
+own."""
+import json
 import os
 import subprocess
+import sys
 
 import pytest
 
 import oracle
-import pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "pkv_oracle.c")
+PINS = os.path.join(os.path.dirname(os.path.abspath(__file__)), "pins.py")
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 # (name, text to replace, replacement, which occurrence (0-based))
 MUTANTS = [
@@ -52,15 +56,17 @@ def test_mutant_is_caught(tmp_path, name, old, new, nth):
     c.write_text(mutated)
     subprocess.run(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fPIC", "-shared",
                     "-o", str(so), str(c), "-lm"], check=True)
-    saved = oracle._lib
-    oracle._lib = oracle.load(so)
-    failed = []
-    try:
-        for pin in pins.ALL_PINS:
-            try:
-                pin()
-            except (AssertionError, ValueError):
-                failed.append(pin.__name__)
-    finally:
-        oracle._lib = saved
-    assert failed, f"no pin caught the planted mistake: {name}"
+    # each mutant runs in a process of its own: a planted mistake may write
+    # out of bounds or crash, and must not corrupt this process
+    r = subprocess.run([sys.executable, PINS, str(so)], capture_output=True, text=True, timeout=300,
+                       cwd=ROOT, env={**os.environ, "PYTHONPATH": os.pathsep.join([ROOT, os.path.dirname(PINS)])})
+    caught = r.returncode != 0 or bool(json.loads(r.stdout.strip().splitlines()[-1]))
+    assert caught, f"no pin caught the planted mistake: {name}"
+
+
+def test_unmutated_oracle_passes_in_a_subprocess():
+    r = subprocess.run([sys.executable, PINS, str(oracle.build())], capture_output=True, text=True,
+                       timeout=300, cwd=ROOT,
+                       env={**os.environ, "PYTHONPATH": os.pathsep.join([ROOT, os.path.dirname(PINS)])})
+    assert r.returncode == 0, r.stderr
+    assert json.loads(r.stdout.strip().splitlines()[-1]) == []
