@@ -103,9 +103,15 @@ pkv_status kv_reshape_and_cache(const void *key_dev, const void *value_dev,
  *                     within a context latches PKV_EINDEX.  Entries past
  *                     ceil(n / B) are never read.
  *   workspace_dev     at least paged_attention_workspace_size(...) bytes of
- *                     device scratch owned by the caller (may be NULL when
- *                     that size is 0); its contents need no initialisation
- *                     and are clobbered.
+ *                     device scratch owned by the caller, initialised once
+ *                     with paged_attention_workspace_init before its first
+ *                     use.  Its head holds the work-ticket counters, which
+ *                     every completed call leaves ready for the next; the
+ *                     rest is clobbered.  Calls that may overlap on the GPU
+ *                     need separate workspaces.  After a call that reported
+ *                     PKV_ETIMEOUT, initialise it again.  An uninitialised
+ *                     workspace makes the call do nothing and pkv_check
+ *                     report PKV_EINVAL.
  * head_dim in {64, 128}; block_size a power of two in [4, 128];
  * num_heads % num_kv_heads == 0.
  * ------------------------------------------------------------------------- */
@@ -136,11 +142,13 @@ pkv_status paged_attention_decode(void *out_dev, const void *query_dev,
  * paged_attention_decode.
  *   - Sizes whose partials would exceed 16 MiB (see
  *     paged_attention_workspace_size) return PKV_EINVAL, launching nothing.
- *   - The first call on each device looks up the array's device address (no
- *     allocation); make that first call before any stream capture.
+ *   - The first call on each device looks up the array's device address and
+ *     prepares its counters (no allocation; one small kernel on `stream`);
+ *     make that first call before any stream capture.
  *   - All calls on a device share the one array: calls that may overlap on
  *     the GPU (other streams, other threads) race and give wrong results; one
- *     call at a time per device.  The array needs no clearing between calls.
+ *     call at a time per device.  Each completed call leaves the array ready
+ *     for the next; after PKV_ETIMEOUT the library cannot reuse it.
  * ------------------------------------------------------------------------- */
 pkv_status paged_attention_decode_noalloc(void *out_dev, const void *query_dev,
                                           const void *key_cache_dev, const void *value_cache_dev,
@@ -152,11 +160,17 @@ pkv_status paged_attention_decode_noalloc(void *out_dev, const void *query_dev,
                                           int partition_size, pkv_dtype dtype,
                                           struct CUstream_st *stream);
 
-/* Bytes of workspace paged_attention_decode needs for these sizes (0 when no
- * context can span more than one partition).  partition_size as above. */
+/* Bytes of workspace paged_attention_decode needs for these sizes: 256 for
+ * the counters, plus the partition partials when a context can span more
+ * than one partition.  partition_size as above. */
 size_t paged_attention_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
                                       int head_dim, int max_context_len,
                                       int partition_size);
+
+/* Prepare a workspace for paged_attention_decode (asynchronous on `stream`;
+ * one small kernel).  workspace_bytes >= 256. */
+pkv_status paged_attention_workspace_init(void *workspace_dev, size_t workspace_bytes,
+                                          struct CUstream_st *stream);
 
 /* The partition size paged_attention_decode uses for these arguments. */
 int paged_attention_partition_size(int num_seqs, int num_heads, int num_kv_heads,
@@ -191,8 +205,9 @@ pkv_status pkv_validate_copy_pairs(const int32_t *src_dst_pairs_host, int num_pa
  * ------------------------------------------------------------------------- */
 
 /* Synchronise `stream`, then report and clear the error latched on the
- * current device (PKV_OK, PKV_EINDEX or PKV_ETIMEOUT; PKV_ECUDA when the
- * stream itself failed). */
+ * current device (PKV_OK, PKV_EINDEX, PKV_ETIMEOUT, or PKV_EINVAL for an
+ * attention workspace that was not initialised; PKV_ECUDA when the stream
+ * itself failed). */
 pkv_status pkv_check(struct CUstream_st *stream);
 
 /* Message for the last failing call of this thread (never NULL). */

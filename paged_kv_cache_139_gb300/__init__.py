@@ -24,7 +24,7 @@ import torch
 from ._lib import STATUS, load
 
 __all__ = ["PkvError", "PkvOOM", "kv_reshape_and_cache", "paged_attention_decode",
-           "paged_attention_decode_noalloc", "paged_attention_workspace_size",
+           "paged_attention_decode_noalloc", "paged_attention_workspace_size", "make_workspace",
            "paged_attention_partition_size", "copy_blocks",
            "validate_copy_pairs", "check", "launch_count", "version", "BlockAllocator", "library_path"]
 
@@ -121,15 +121,25 @@ def paged_attention_partition_size(num_seqs: int, num_heads: int, num_kv_heads: 
                                                      max_context_len, partition_size))
 
 
+def make_workspace(device, nbytes: int, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """A device buffer of at least nbytes, prepared for paged_attention_decode
+    (paged_attention_workspace_init)."""
+    dev = torch.device(device)
+    buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+    _ck(load().paged_attention_workspace_init(buf.data_ptr(), buf.numel(), _stream(stream, dev)),
+        "paged_attention_workspace_init")
+    return buf
+
+
 _ws_cache: dict = {}
 
 
 def _workspace(device, nbytes: int) -> torch.Tensor:
-    """A device scratch buffer of at least nbytes, kept per device."""
+    """The binding's own workspace: at least nbytes, kept per device."""
     key = torch.device(device)
     buf = _ws_cache.get(key)
     if buf is None or buf.numel() < nbytes:
-        buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=key)
+        buf = make_workspace(key, nbytes)
         _ws_cache[key] = buf
     return buf
 
@@ -141,7 +151,9 @@ def paged_attention_decode(out: torch.Tensor, query: torch.Tensor, key_cache: to
                            workspace: Optional[torch.Tensor] = None,
                            stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
     """out/query [S][H][d]; caches [NB][Hkv][B][d]; block_tables int32 [S][MB];
-    context_lens int32 [S].  scale defaults to 1/sqrt(d).  Returns out."""
+    context_lens int32 [S].  scale defaults to 1/sqrt(d).  A workspace passed
+    in must come from make_workspace (or paged_attention_workspace_init) and
+    serve one call at a time.  Returns out."""
     S, H, d = query.shape
     NB, Hkv, B, d2 = key_cache.shape
     if d2 != d or out.shape != query.shape or value_cache.shape != key_cache.shape:
@@ -154,11 +166,10 @@ def paged_attention_decode(out: torch.Tensor, query: torch.Tensor, key_cache: to
     mcl = max_context_len if max_context_len > 0 else mb * B
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    need = paged_attention_workspace_size(S, H, Hkv, d, mcl, partition_size)
     if workspace is None:
-        workspace = _workspace(query.device, need) if need else None
-    ws_ptr = _dev(workspace, "workspace") if workspace is not None else None
-    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+        workspace = _workspace(query.device, paged_attention_workspace_size(S, H, Hkv, d, mcl, partition_size))
+    ws_ptr = _dev(workspace, "workspace")
+    ws_bytes = workspace.numel() * workspace.element_size()
     rc = load().paged_attention_decode(
         _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
         _dev(block_tables, "block_tables", torch.int32), _dev(context_lens, "context_lens", torch.int32),

@@ -157,6 +157,8 @@ struct AttnArgs {
     const int32_t *tables;       // [S][max_blocks]
     const int32_t *ctx_lens;     // [S]
     DeviceStatus *st;
+    struct WsHeader *hdr;        // work-ticket counters at the head of the workspace
+    int num_seqs;
     int max_blocks;
     int max_ctx;
     int log2_block;
@@ -369,6 +371,369 @@ __global__ void __launch_bounds__(kThreads, min_ctas<G>()) paged_attention_kerne
     }
 }
 
+// ---------------------------------------------------------------------------
+// Persistent variant.  One or two CTAs per SM stay resident and claim work
+// items -- (sequence, partition, query-head tile), in that order -- with
+// tickets from a counter at the head of the workspace.  Each CTA first turns
+// the context lengths into a prefix sum of partitions per sequence in shared
+// memory, so a ticket maps to a real item with one binary search and no
+// empty CTA is ever launched.  The ring keeps streaming across items; an
+// item's stages are padded to a multiple of the consumer-warp count so that
+// every warp takes part in every item's merge, which goes through shared
+// memory and an mbarrier (bounded waits only, no named barriers).
+// ---------------------------------------------------------------------------
+
+struct WsHeader {
+    unsigned int next;        // next ticket
+    unsigned int done;        // CTAs that have taken their last ticket
+    unsigned int magic;       // kWsMagic once paged_attention_workspace_init has run
+    unsigned int pad;
+};
+constexpr unsigned int kWsMagic = 0x31766b70u;
+constexpr size_t kWsHeaderBytes = 256;
+constexpr int kMaxPersistentSeqs = 4096;      // sequence tables kept in shared memory
+
+enum : int { kMetaFirst = 1, kMetaLast = 2, kMetaStop = 4 };
+
+struct StageMeta {
+    int s, h0, part, nparts;  // the work item
+    int nvalid;               // tokens in the stage (0: padding)
+    int flags;                // kMeta*
+    int qbuf;                 // query buffer of the item
+    int pad;
+};
+
+template <int D, int G, typename T> struct PLayout {
+    using Gm = Geometry<D>;
+    static constexpr int NQ = Gm::NSTAGE / kConsumerWarps;            // query buffers (see the producer)
+    static constexpr size_t ring = 0;
+    static constexpr size_t qs = ring + (size_t)Gm::NSTAGE * 2 * Gm::STAGE_ELEMS * sizeof(T);
+    static constexpr size_t merge = qs + (size_t)NQ * kConsumerWarps * G * D * sizeof(T);
+    static constexpr size_t bars = merge + (size_t)2 * kConsumerWarps * G * (D + 2) * sizeof(float);
+    static constexpr size_t meta = bars + (size_t)(2 * Gm::NSTAGE + 2) * sizeof(uint64_t);
+    static constexpr size_t seqs = meta + (size_t)Gm::NSTAGE * sizeof(StageMeta);
+    static size_t bytes(int S) { return seqs + (size_t)(2 * S + 1) * sizeof(int); }
+};
+
+// In place: v[1..n] := inclusive prefix sums of v[1..n]; v[0] := 0.
+__device__ __forceinline__ void block_prefix_sum(int *v, int n) {
+    __shared__ int warp_tot[32];
+    const int nt = blockDim.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int chunk = (n + nt - 1) / nt;
+    const int b0 = tid * chunk < n ? tid * chunk : n;
+    const int b1 = b0 + chunk < n ? b0 + chunk : n;
+    int sum = 0;
+    for (int i = b0; i < b1; i++) sum += v[i + 1];
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_tot[wid] = incl;
+    __syncthreads();
+    int off = 0;
+    for (int w = 0; w < wid; w++) off += warp_tot[w];
+    int run = off + incl - sum;
+    for (int i = b0; i < b1; i++) {
+        run += v[i + 1];
+        v[i + 1] = run;
+    }
+    if (tid == 0) v[0] = 0;
+    __syncthreads();
+}
+
+template <int D, int G, typename T>
+__global__ void __launch_bounds__(kThreads, 2) paged_attention_persistent_kernel(const AttnArgs a) {
+    using Gm = Geometry<D>;
+    using L = PLayout<D, G, T>;
+    constexpr int NSTAGE = Gm::NSTAGE, SE = Gm::STAGE_ELEMS, LPR = Gm::LPR, W = kConsumerWarps;
+    constexpr int NQ = L::NQ;
+    extern __shared__ __align__(128) unsigned char smem[];
+    T *ring = reinterpret_cast<T *>(smem + L::ring);                 // [NSTAGE][2][32][D]
+    T *qs = reinterpret_cast<T *>(smem + L::qs);                     // [NQ][W][G][D]
+    float *mg = reinterpret_cast<float *>(smem + L::merge);          // [2][W][G][D + 2]: o, m, l
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::bars);
+    uint64_t *empty = full + NSTAGE;
+    uint64_t *mbar = empty + NSTAGE;                                 // [2] item merges
+    StageMeta *meta = reinterpret_cast<StageMeta *>(smem + L::meta);
+    const int S = a.num_seqs;
+    int *pref = reinterpret_cast<int *>(smem + L::seqs);             // [S + 1] partitions before s
+    int *ctxs = pref + S + 1;                                        // [S]
+    __shared__ int cta_flags;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tiles = a.num_kv_heads * a.head_tiles;
+    WsHeader *hdr = a.hdr;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NSTAGE; i++) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        mbar_init(&mbar[0], W * 32);
+        mbar_init(&mbar[1], W * 32);
+        fence_mbar_init();
+    }
+    pdl_trigger();
+    pdl_wait();
+    if (threadIdx.x == 0) cta_flags = (timed_out(a.st) ? 1 : 0) | (hdr->magic != kWsMagic ? 2 : 0);
+    for (int i = threadIdx.x; i < S; i += blockDim.x) {
+        int c = a.ctx_lens[i];
+        if (c < 0 || c > a.max_ctx) {
+            if (blockIdx.x == 0) latch(a.st, kFlagBadContext, c);
+            c = c < 0 ? 0 : a.max_ctx;
+        }
+        ctxs[i] = c;
+        pref[i + 1] = c > 0 ? (c + a.partition - 1) / a.partition : 1;
+    }
+    __syncthreads();
+    if (cta_flags) {                                   // uniform over the CTA
+        if ((cta_flags & 2) && blockIdx.x == 0 && threadIdx.x == 0) latch(a.st, kFlagBadWorkspace, hdr->magic);
+        return;
+    }
+    block_prefix_sum(pref, S);
+    const unsigned int N = (unsigned int)pref[S] * (unsigned int)tiles;
+    const int B = 1 << a.log2_block;
+
+    if (warp == W) {
+        // ---------------- producer: tickets -> items -> bulk copies ----------------
+        const T *kc = static_cast<const T *>(a.k_cache);
+        const T *vc = static_cast<const T *>(a.v_cache);
+        const T *qg = static_cast<const T *>(a.q);
+        const int cps = B >= kStageRows ? 1 : kStageRows >> a.log2_block;
+        const int rows_per_copy = B >= kStageRows ? kStageRows : B;
+        const uint32_t copy_bytes = (uint32_t)(rows_per_copy * D * sizeof(T));
+        const uint32_t q_bytes = (uint32_t)(G * D * sizeof(T));
+        const uint64_t policy = policy_evict_first();
+        unsigned int ticket = 0;
+        if (lane == 0) ticket = atomicAdd(&hdr->next, 1u);
+        ticket = __shfl_sync(kFull, ticket, 0);
+        int kk = 0, items = 0;
+        bool dead = false;
+        while (ticket < N && !dead) {
+            unsigned int nxt = 0;
+            if (lane == 0) nxt = atomicAdd(&hdr->next, 1u);      // the next item's ticket, used below
+            const int pidx = (int)(ticket / (unsigned int)tiles);
+            const int tile = (int)(ticket % (unsigned int)tiles);
+            int lo = 0, hi = S;                                    // pref[lo] <= pidx < pref[hi]
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (pref[mid] <= pidx) lo = mid; else hi = mid;
+            }
+            const int s = lo, part = pidx - pref[s], nparts = pref[s + 1] - pref[s];
+            const int g = tile / a.head_tiles;
+            const int h0 = g * (a.head_tiles * G) + (tile % a.head_tiles) * G;
+            const int ctx = ctxs[s];
+            const int tok0 = part * a.partition;
+            int ntok = ctx - tok0 < a.partition ? ctx - tok0 : a.partition;
+            if (ntok < 0) ntok = 0;
+            const int nst = (ntok + kStageRows - 1) / kStageRows;
+            const int npad = ((nst > 0 ? nst : 1) + W - 1) / W * W;
+            const int32_t *trow = a.tables + (size_t)s * a.max_blocks;
+            const int nblk = (ctx + B - 1) >> a.log2_block;
+            // Query buffer: written with the item's first W stages; with NQ =
+            // NSTAGE / W buffers and every item at least W stages long, a
+            // buffer is rewritten only after its previous item's first stages
+            // have been consumed.
+            const int qb = items % NQ;
+            int win = -(1 << 30), ent = -1;
+            for (int i = 0; i < npad; i++, kk++) {
+                int e[8];
+                int off0 = 0;
+                if (i < nst) {                                     // uniform over the warp
+                    const int t_first = tok0 + i * kStageRows;
+                    const int lb0 = t_first >> a.log2_block;
+                    off0 = t_first & (B - 1);
+                    if (lb0 < win || lb0 + cps > win + 32) {
+                        win = lb0;
+                        const int j = win + lane;
+                        ent = j < nblk ? __ldg(trow + j) : -1;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; j++) e[j] = __shfl_sync(kFull, ent, (lb0 + j - win) & 31);
+                }
+                if (lane == 0) {
+                    const int slot = kk % NSTAGE;
+                    if (kk >= NSTAGE && !mbar_wait(&empty[slot], ((kk / NSTAGE) - 1) & 1, kWaitLimitCycles)) {
+                        latch(a.st, kFlagTimeout, kk);
+                        dead = true;
+                    }
+                    if (!dead) {
+                        int nv = 0, ncopies = 0;
+                        if (i < nst) {
+                            nv = ntok - i * kStageRows < kStageRows ? ntok - i * kStageRows : kStageRows;
+                            for (int j = 0; j < cps && j < 8; j++) {
+                                if (j * rows_per_copy >= nv) break;
+                                const int p = e[j];
+                                if (p < 0 || p >= a.num_blocks) {
+                                    latch(a.st, kFlagBadBlock, p);
+                                    nv = j * rows_per_copy;
+                                    break;
+                                }
+                                ncopies = j + 1;
+                            }
+                        }
+                        const bool withq = i < W && i < nst;       // warp i's first stage of the item
+                        StageMeta &m = meta[slot];
+                        m.s = s;
+                        m.h0 = h0;
+                        m.part = part;
+                        m.nparts = nparts;
+                        m.nvalid = nv;
+                        m.qbuf = qb;
+                        m.flags = (i < W ? kMetaFirst : 0) | (i >= npad - W ? kMetaLast : 0);
+                        mbar_arrive_expect_tx(&full[slot], 2u * copy_bytes * (uint32_t)ncopies + (withq ? q_bytes : 0u));
+                        if (withq)
+                            bulk_g2s(qs + (size_t)(qb * W + i) * G * D, qg + ((size_t)s * a.num_heads + h0) * D,
+                                     q_bytes, &full[slot]);
+                        for (int j = 0; j < ncopies; j++) {
+                            const size_t goff = (((size_t)e[j] * a.num_kv_heads + g) * B + off0) * D;
+                            T *dk = ring + (size_t)(slot * 2) * SE + (size_t)j * rows_per_copy * D;
+                            bulk_g2s_hint(dk, kc + goff, copy_bytes, &full[slot], policy);
+                            bulk_g2s_hint(dk + SE, vc + goff, copy_bytes, &full[slot], policy);
+                        }
+                    }
+                }
+                dead = __shfl_sync(kFull, dead ? 1 : 0, 0) != 0;
+                if (dead) break;
+            }
+            items++;
+            ticket = __shfl_sync(kFull, nxt, 0);
+        }
+        if (lane == 0) {
+            // one stop mark per consumer warp
+            for (int w = 0; w < W && !dead; w++, kk++) {
+                const int slot = kk % NSTAGE;
+                if (kk >= NSTAGE && !mbar_wait(&empty[slot], ((kk / NSTAGE) - 1) & 1, kWaitLimitCycles)) {
+                    latch(a.st, kFlagTimeout, kk);
+                    dead = true;
+                    break;
+                }
+                meta[slot].flags = kMetaStop;
+                mbar_arrive_expect_tx(&full[slot], 0u);
+            }
+            // the last CTA to finish leaves the counters at zero for the next call
+            __threadfence();
+            if (atomicAdd(&hdr->done, 1u) == gridDim.x - 1) {
+                hdr->next = 0;
+                hdr->done = 0;
+                __threadfence();
+            }
+        }
+        return;
+    }
+
+    // ---------------- consumers ----------------
+    const int r = lane / LPR, c = lane % LPR;
+    float qf[G][8], m[G], lsum[G], acc[G][8];
+#pragma unroll
+    for (int h = 0; h < G; h++) {
+        m[h] = -INFINITY;
+        lsum[h] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; e++) acc[h][e] = 0.f;
+    }
+    int jitem = 0;
+    for (int k = warp;; k += W) {
+        const int slot = k % NSTAGE;
+        const bool ok = __all_sync(kFull, mbar_wait(&full[slot], (k / NSTAGE) & 1, kWaitLimitCycles));
+        if (!ok) {
+            if (lane == 0) latch(a.st, kFlagTimeout, k);
+            break;
+        }
+        const StageMeta md = meta[slot];
+        if (md.flags & kMetaStop) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+            break;
+        }
+        if ((md.flags & kMetaFirst) && md.nvalid > 0) {
+            const T *qp = qs + (size_t)(md.qbuf * W + warp) * G * D + c * 8;
+#pragma unroll
+            for (int h = 0; h < G; h++) {
+                const uint4 raw = *reinterpret_cast<const uint4 *>(qp + h * D);
+                F16Traits<T>::to_f32(raw, qf[h]);
+#pragma unroll
+                for (int e = 0; e < 8; e++) qf[h][e] *= a.scale_log2;
+            }
+        }
+        const T *Ks = ring + (size_t)(slot * 2) * SE;
+        if (md.nvalid == kStageRows)
+            consume_stage<D, G, T, true>(Ks, Ks + SE, md.nvalid, r, c, qf, m, lsum, acc);
+        else if (md.nvalid > 0)
+            consume_stage<D, G, T, false>(Ks, Ks + SE, md.nvalid, r, c, qf, m, lsum, acc);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        if (!(md.flags & kMetaLast)) continue;
+
+        // ---- the item's merge: this warp's state into buffer b, then W-way combine ----
+        const int b = jitem & 1;
+#pragma unroll
+        for (int h = 0; h < G; h++) {
+            lsum[h] = warp_sum(lsum[h]);
+#pragma unroll
+            for (int e = 0; e < 8; e++) {
+#pragma unroll
+                for (int o = LPR; o < 32; o <<= 1) acc[h][e] += __shfl_xor_sync(kFull, acc[h][e], o);
+            }
+        }
+        float *mw = mg + (size_t)(b * W + warp) * G * (D + 2);
+        if (r == 0) {
+#pragma unroll
+            for (int h = 0; h < G; h++)
+#pragma unroll
+                for (int e = 0; e < 8; e++) mw[h * (D + 2) + c * 8 + e] = acc[h][e];
+        }
+        if (lane == 0) {
+#pragma unroll
+            for (int h = 0; h < G; h++) {
+                mw[h * (D + 2) + D] = m[h];
+                mw[h * (D + 2) + D + 1] = lsum[h];
+            }
+        }
+        mbar_arrive(&mbar[b]);                                   // every lane, after its own writes
+        if (!__all_sync(kFull, mbar_wait(&mbar[b], (jitem >> 1) & 1, kWaitLimitCycles))) {
+            if (lane == 0) latch(a.st, kFlagTimeout, -1 - jitem);
+            break;
+        }
+        const float *mb = mg + (size_t)b * W * G * (D + 2);
+        for (int idx = warp * 32 + lane; idx < G * D; idx += W * 32) {
+            const int h = idx / D, e = idx % D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < W; w++) M = fmaxf(M, mb[(w * G + h) * (D + 2) + D]);
+            float Lsum = 0.f, O = 0.f;
+#pragma unroll
+            for (int w = 0; w < W; w++) {
+                const float *x = mb + (w * G + h) * (D + 2);
+                const float wt = x[D] == -INFINITY ? 0.f : exp2f(x[D] - M);
+                Lsum = fmaf(x[D + 1], wt, Lsum);
+                O = fmaf(x[e], wt, O);
+            }
+            const size_t sh = (size_t)md.s * a.num_heads + md.h0 + h;
+            if (md.nparts <= 1) {
+                static_cast<T *>(a.out)[sh * D + e] = F16Traits<T>::from_f32(Lsum > 0.f ? O / Lsum : 0.f);
+            } else {
+                const size_t sp = sh * a.max_parts + md.part;
+                a.ws_o[sp * D + e] = O;
+                if (e == 0) {
+                    a.ws_m[sp] = M;
+                    a.ws_l[sp] = Lsum;
+                }
+            }
+        }
+        jitem++;
+#pragma unroll
+        for (int h = 0; h < G; h++) {
+            m[h] = -INFINITY;
+            lsum[h] = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; e++) acc[h][e] = 0.f;
+        }
+    }
+}
+
 // Merge the partitions of each (sequence, head) with more than one:
 // M = max_p m_p, L = sum_p l_p 2^(m_p - M), out = sum_p o_p 2^(m_p - M) / L.
 template <int D, typename T>
@@ -407,19 +772,46 @@ struct WsLayout {
     size_t m_off, l_off, o_off, bytes;
 };
 
+// Workspace: the ticket header, then (when contexts may span partitions)
+// m, l [S][H][MP] and o [S][H][MP][D], each 256-byte aligned.
 WsLayout ws_layout(int S, int H, int D, int MP) {
     WsLayout w{};
+    w.bytes = kWsHeaderBytes;
     if (MP <= 1) return w;
     const size_t n = (size_t)S * H * MP;
-    w.m_off = 0;
-    w.l_off = align256(n * sizeof(float));
+    w.m_off = kWsHeaderBytes;
+    w.l_off = w.m_off + align256(n * sizeof(float));
     w.o_off = w.l_off + align256(n * sizeof(float));
     w.bytes = w.o_off + align256(n * D * sizeof(float));
     return w;
 }
 
+__global__ void workspace_init_kernel(WsHeader *h) {
+    pdl_trigger();
+    pdl_wait();
+    h->next = 0;
+    h->done = 0;
+    h->pad = 0;
+    h->magic = kWsMagic;
+}
+
 template <int D, int G, typename T> cudaError_t launch_attention(const AttnArgs &a, dim3 grid, cudaStream_t st) {
-    static bool configured = false;      // per template instance; harmless if repeated
+    if (a.num_seqs <= kMaxPersistentSeqs) {
+        static bool configured_p = false;    // per template instance; harmless if repeated
+        auto kern = paged_attention_persistent_kernel<D, G, T>;
+        if (!configured_p) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)PLayout<D, G, T>::bytes(kMaxPersistentSeqs));
+            if (e != cudaSuccess) return e;
+            configured_p = true;
+        }
+        // enough CTAs to fill the GPU, never more than there can be items
+        const long long items = (long long)grid.x * grid.y * grid.z;
+        long long ctas = (long long)sm_count() * 2;
+        if (ctas > items) ctas = items;
+        return launch(kern, dim3((unsigned)ctas), dim3(kThreads), PLayout<D, G, T>::bytes(a.num_seqs), st, a);
+    }
+    static bool configured = false;
     auto kern = paged_attention_kernel<D, G, T>;
     const size_t smem = smem_bytes<D, T>();
     if (!configured) {
@@ -462,10 +854,21 @@ int paged_attention_partition_size(int num_seqs, int num_heads, int num_kv_heads
     return pkv::choose_partition(partition_size);
 }
 
+pkv_status paged_attention_workspace_init(void *workspace, size_t workspace_bytes, struct CUstream_st *stream) {
+    using namespace pkv;
+    if (!workspace || workspace_bytes < kWsHeaderBytes || !aligned16(workspace))
+        return fail(PKV_EINVAL, "paged_attention_workspace_init: need a 16-byte aligned workspace of at least %zu bytes",
+                    kWsHeaderBytes);
+    cudaError_t e = launch(workspace_init_kernel, dim3(1), dim3(1), 0, stream, static_cast<WsHeader *>(workspace));
+    if (e != cudaSuccess) return fail(PKV_ECUDA, "paged_attention_workspace_init: launch: %s", cudaGetErrorString(e));
+    return PKV_OK;
+}
+
 size_t paged_attention_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
                                       int max_context_len, int partition_size) {
-    if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_context_len <= 0 || partition_size < 0)
+    if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_context_len < 0 || partition_size < 0)
         return 0;
+    if (max_context_len == 0) return pkv::kWsHeaderBytes;
     const int P = paged_attention_partition_size(num_seqs, num_heads, num_kv_heads, head_dim, max_context_len,
                                                  partition_size);
     return pkv::ws_layout(num_seqs, num_heads, head_dim, pkv::parts_for(max_context_len, P)).bytes;
@@ -506,7 +909,7 @@ pkv_status paged_attention_decode(void *out, const void *query, const void *key_
     const int MP = parts_for(max_ctx, P);
     if (MP > 65535) return fail(PKV_EINVAL, "paged_attention_decode: %d partitions per sequence", MP);
     const WsLayout wl = ws_layout(num_seqs, num_heads, head_dim, MP);
-    if (wl.bytes > 0 && (!workspace || workspace_bytes < wl.bytes || !aligned16(workspace)))
+    if (!workspace || workspace_bytes < wl.bytes || !aligned16(workspace))
         return fail(PKV_EINVAL, "paged_attention_decode: workspace of %zu bytes needed, %zu given", wl.bytes,
                     workspace ? workspace_bytes : (size_t)0);
     DeviceStatus *st = status_ptr();
@@ -517,9 +920,11 @@ pkv_status paged_attention_decode(void *out, const void *query, const void *key_
     AttnArgs a;
     a.out = out;
     unsigned char *ws = static_cast<unsigned char *>(workspace);
-    a.ws_m = wl.bytes ? reinterpret_cast<float *>(ws + wl.m_off) : nullptr;
-    a.ws_l = wl.bytes ? reinterpret_cast<float *>(ws + wl.l_off) : nullptr;
-    a.ws_o = wl.bytes ? reinterpret_cast<float *>(ws + wl.o_off) : nullptr;
+    a.hdr = reinterpret_cast<WsHeader *>(ws);
+    a.ws_m = MP > 1 ? reinterpret_cast<float *>(ws + wl.m_off) : nullptr;
+    a.ws_l = MP > 1 ? reinterpret_cast<float *>(ws + wl.l_off) : nullptr;
+    a.ws_o = MP > 1 ? reinterpret_cast<float *>(ws + wl.o_off) : nullptr;
+    a.num_seqs = num_seqs;
     a.q = query;
     a.k_cache = key_cache;
     a.v_cache = value_cache;

@@ -32,8 +32,10 @@ void *g_scratch_addr[kMaxDevices] = {};
 
 // Device address of g_scratch on the current device.  In host code the name
 // g_scratch is only a host-side stand-in for the symbol, never a device
-// address, so the address is looked up once per device and cached.
-void *scratch_address(pkv_status *st) {
+// address, so the address is looked up once per device and cached; the same
+// set-up prepares the array's counters (a kernel on the caller's stream,
+// ordered before the first attention launch).
+void *scratch_address(cudaStream_t stream, pkv_status *st) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -48,6 +50,11 @@ void *scratch_address(pkv_status *st) {
         if (e != cudaSuccess || !p) {
             *st = pkv::fail(PKV_ECUDA, "paged_attention_decode_noalloc: scratch address on device %d: %s", dev,
                             cudaGetErrorString(e));
+            return nullptr;
+        }
+        const pkv_status ist = paged_attention_workspace_init(p, kScratchBytes, stream);
+        if (ist != PKV_OK) {
+            *st = ist;
             return nullptr;
         }
         g_scratch_addr[dev] = p;
@@ -73,14 +80,10 @@ extern "C" pkv_status paged_attention_decode_noalloc(
                          "paged_attention_decode_noalloc: these sizes need %zu bytes of partition scratch; the "
                          "built-in scratch holds %zu (use paged_attention_decode with a caller workspace)",
                          need, kScratchBytes);
-    void *ws = nullptr;
-    if (need > 0) {
-        pkv_status st = PKV_OK;
-        ws = scratch_address(&st);
-        if (!ws) return st;
-    }
+    pkv_status st = PKV_OK;
+    void *ws = scratch_address(stream, &st);
+    if (!ws) return st;
     return paged_attention_decode(out, query, key_cache, value_cache, block_tables, context_lens, num_seqs,
                                   max_blocks_per_seq, max_context_len, block_size, num_blocks, num_heads,
-                                  num_kv_heads, head_dim, scale, partition_size, ws, ws ? kScratchBytes : 0,
-                                  dtype, stream);
+                                  num_kv_heads, head_dim, scale, partition_size, ws, kScratchBytes, dtype, stream);
 }

@@ -27,6 +27,7 @@ enum : unsigned int {
     kFlagBadPair = 4u,         // copy pair with a block id outside the pool
     kFlagTimeout = 8u,         // a bounded wait gave up
     kFlagBadContext = 16u,     // context length negative or beyond the table
+    kFlagBadWorkspace = 32u,   // attention workspace not initialised
 };
 
 __device__ __forceinline__ void latch(DeviceStatus *st, unsigned int flag, long long value) {

@@ -99,6 +99,9 @@ pkv_status pkv_check(struct CUstream_st *stream) {
     std::memset(&zero, 0, sizeof zero);
     e = cudaMemcpyToSymbol(pkv::g_status, &zero, sizeof zero);
     if (e != cudaSuccess) return pkv::fail(PKV_ECUDA, "pkv_check: clearing status: %s", cudaGetErrorString(e));
+    if (h.flags & pkv::kFlagBadWorkspace)
+        return pkv::fail(PKV_EINVAL, "device error flags 0x%x: attention workspace not initialised "
+                                     "(paged_attention_workspace_init)", h.flags);
     const char *what = (h.first_flag & pkv::kFlagBadSlot)      ? "slot outside the pool"
                        : (h.first_flag & pkv::kFlagBadBlock)   ? "block-table entry outside the pool"
                        : (h.first_flag & pkv::kFlagBadPair)    ? "copy pair outside the pool"

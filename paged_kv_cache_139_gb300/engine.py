@@ -16,7 +16,7 @@ from typing import Optional, Sequence
 import numpy as np
 import torch
 
-from . import (BlockAllocator, copy_blocks, kv_reshape_and_cache, paged_attention_decode,
+from . import (BlockAllocator, copy_blocks, kv_reshape_and_cache, make_workspace, paged_attention_decode,
                paged_attention_workspace_size)
 
 
@@ -95,10 +95,8 @@ class PagedKVCache:
     def workspace(self, num_seqs: int, num_heads: int, max_context_len: int, partition_size: int = 0):
         need = paged_attention_workspace_size(num_seqs, num_heads, self.num_kv_heads, self.head_dim,
                                               max_context_len, partition_size)
-        if need == 0:
-            return None
         if self._ws is None or self._ws.numel() < need:
-            self._ws = torch.empty(need, dtype=torch.uint8, device=self.device)
+            self._ws = make_workspace(self.device, need)
         return self._ws
 
     def copy_on_write(self, pairs: torch.Tensor) -> None:

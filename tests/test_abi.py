@@ -68,7 +68,7 @@ def test_attention_workspace_needed():
     # 4 blocks of 16 = 64 tokens and partitions of 32: two partitions -> workspace required
     assert pkv.paged_attention_workspace_size(2, 4, 2, 128, 64, 32) > 0
     assert _call_attention(P=32) == 1
-    assert pkv.paged_attention_workspace_size(2, 4, 2, 128, 64, 64) == 0
+    assert pkv.paged_attention_workspace_size(2, 4, 2, 128, 64, 64) == 256     # the counters only
 
 
 def test_workspace_size_formula():
@@ -76,7 +76,14 @@ def test_workspace_size_formula():
     S, H, d, ctx, P = 8, 32, 128, 32768, 512
     n = S * H * (ctx // P)
     r = lambda x: (x + 255) // 256 * 256
-    assert pkv.paged_attention_workspace_size(S, H, 8, d, ctx, P) == r(4 * n) * 2 + r(4 * n * d)
+    assert pkv.paged_attention_workspace_size(S, H, 8, d, ctx, P) == 256 + r(4 * n) * 2 + r(4 * n * d)
+
+
+def test_workspace_init_rejects_bad_arguments():
+    L = _lib.load()
+    assert L.paged_attention_workspace_init(None, 4096, None) == 1
+    assert L.paged_attention_workspace_init(16, 128, None) == 1        # smaller than the counters
+    assert L.paged_attention_workspace_init(24, 4096, None) == 1       # misaligned
 
 
 def test_cache_write_rejects_bad_arguments():

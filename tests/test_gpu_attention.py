@@ -185,6 +185,28 @@ def test_context_beyond_bound_latches_eindex(cuda_device):
     assert e.value.status_name == "PKV_EINDEX" and "context" in str(e.value)
 
 
+def test_uninitialised_workspace_is_reported(cuda_device):
+    w = _custom(ctx=(50, 90), S=2)
+    c = Case(w, cuda_device)
+    ws = torch.zeros(4096, dtype=torch.uint8, device=cuda_device)          # never initialised
+    out = torch.full_like(c.q_dev, 3.0)
+    pkv.paged_attention_decode(out, c.q_dev, c.eng.key_cache, c.eng.value_cache, c.dev.tables,
+                               c.dev.context_lens, workspace=ws)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.check()
+    assert e.value.status_name == "PKV_EINVAL" and "workspace" in str(e.value)
+    assert bool((out == 3.0).all())                                          # nothing was written
+
+
+def test_repeated_calls_reuse_the_workspace(cuda_device):
+    """The ticket counters reset themselves: many calls on one workspace give
+    identical results."""
+    w = _custom(H=8, Hkv=2, ctx=(5, 900, 1500, 31), S=4)
+    c = Case(w, cuda_device, partition_size=128)
+    outs = [c.rerun_attention().clone() for _ in range(5)]
+    assert all(torch.equal(outs[0], o) for o in outs[1:]) and torch.equal(outs[0], c.out)
+
+
 def test_bounded_wait_times_out_and_context_survives(cuda_device):
     L = pkv._lib.load()
     import ctypes
@@ -211,10 +233,11 @@ def test_output_guard_bytes(cuda_device):
 
 
 def test_launch_count_and_native_library(cuda_device):
-    before = pkv.launch_count()
     c = Case(_custom(ctx=(600, 700), S=2, H=4, Hkv=4), cuda_device, partition_size=256)
+    before = pkv.launch_count()
+    c.eng.decode(c.q_dev, c.k_dev, c.v_dev, c.dev, partition_size=256)
     pkv.check()
-    # cache write + attention + partition merge
+    # cache write + attention + partition merge (the workspace exists already)
     assert pkv.launch_count() - before == 3
     import os
     maps = open("/proc/self/maps").read()

@@ -56,8 +56,7 @@ def _noalloc_raw(out, q, kc, vc, bt, cl, partition_size):
 def test_noalloc_matches_workspace_entry(cuda_device, S, H, Hkv, d, B, ctx, dtype, P):
     q, kc, vc, bt, cl = _inputs(cuda_device, S, H, Hkv, d, B, ctx, dtype, 11 + S)
     ref = torch.empty_like(q)
-    ws = torch.empty(max(1, pkv.paged_attention_workspace_size(S, H, Hkv, d, bt.shape[1] * B, P)),
-                     dtype=torch.uint8, device=cuda_device)
+    ws = pkv.make_workspace(cuda_device, pkv.paged_attention_workspace_size(S, H, Hkv, d, bt.shape[1] * B, P))
     pkv.paged_attention_decode(ref, q, kc, vc, bt, cl, partition_size=P, workspace=ws)
     pkv.check()
     want = ref.double().cpu().numpy()
