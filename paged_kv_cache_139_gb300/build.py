@@ -48,11 +48,11 @@ def _stale() -> bool:
     return any(p.stat().st_mtime > t for p in _sources() + _headers() + [pathlib.Path(__file__)])
 
 
-def _compile(src: pathlib.Path, verbose: bool) -> pathlib.Path:
-    obj = OBJ / (src.name + ".o")
+def _compile(src: pathlib.Path, verbose: bool, obj_dir: pathlib.Path = OBJ, defines=()) -> pathlib.Path:
+    obj = obj_dir / (src.name + ".o")
     if src.suffix == ".cu":
         cmd = [_nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
-               "-I", str(INCLUDE), "-I", str(CSRC), "-c", str(src), "-o", str(obj)]
+               "-I", str(INCLUDE), "-I", str(CSRC), *[f"-D{d}" for d in defines], "-c", str(src), "-o", str(obj)]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
     else:
@@ -66,21 +66,25 @@ def _compile(src: pathlib.Path, verbose: bool) -> pathlib.Path:
     return obj
 
 
-def build(force: bool = False, verbose: bool = False) -> pathlib.Path:
-    if not force and not _stale():
+def build(force: bool = False, verbose: bool = False, out: pathlib.Path = None, defines=()) -> pathlib.Path:
+    """Build the library (by default in-tree); `out` and `defines` build a
+    variant with tuning knobs set, elsewhere."""
+    lib = LIB if out is None else pathlib.Path(out)
+    if out is None and not defines and not force and not _stale():
         return LIB
-    OBJ.mkdir(exist_ok=True)
-    LIBDIR.mkdir(exist_ok=True)
+    obj_dir = OBJ if out is None else lib.parent / "_obj"
+    obj_dir.mkdir(parents=True, exist_ok=True)
+    lib.parent.mkdir(parents=True, exist_ok=True)
     with ThreadPoolExecutor(max_workers=len(_sources())) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose), _sources()))
-    tmp = LIBDIR / f"libpkv.{os.getpid()}.so"
+        objs = list(ex.map(lambda s: _compile(s, verbose, obj_dir, defines), _sources()))
+    tmp = lib.parent / f"libpkv.{os.getpid()}.so"
     cmd = [_nvcc(), *ARCH, "-shared", "-o", str(tmp), *map(str, objs), "-lcudart_static", "-lrt", "-ldl",
            "-lpthread"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -34,6 +34,18 @@
 namespace pkv {
 namespace {
 
+// Tuning knobs (compile-time): ring slots per consumer warp for head_dim 128
+// and 64, and resident CTAs per SM of the persistent kernel.
+#ifndef PKV_SLOTS_PER_WARP_D128
+#define PKV_SLOTS_PER_WARP_D128 1
+#endif
+#ifndef PKV_SLOTS_PER_WARP_D64
+#define PKV_SLOTS_PER_WARP_D64 2
+#endif
+#ifndef PKV_PERSISTENT_CTAS_PER_SM
+#define PKV_PERSISTENT_CTAS_PER_SM 2
+#endif
+
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStageRows = 32;              // tokens per ring stage
@@ -47,7 +59,7 @@ template <int D> struct Geometry {
     // Stage k goes to consumer warp k % W and ring slot k % NSTAGE.  NSTAGE is
     // a multiple of W, so every slot belongs to one warp, which waits for its
     // phases in order: a parity wait can never see a phase two ahead.
-    static constexpr int SLOTS_PER_WARP = D >= 128 ? 1 : 2;
+    static constexpr int SLOTS_PER_WARP = D >= 128 ? PKV_SLOTS_PER_WARP_D128 : PKV_SLOTS_PER_WARP_D64;
     static constexpr int NSTAGE = kConsumerWarps * SLOTS_PER_WARP;
     static constexpr int STAGE_ELEMS = kStageRows * D;   // per tensor
     static_assert(NSTAGE % kConsumerWarps == 0, "ring slots must divide among the consumer warps");
@@ -392,6 +404,7 @@ struct WsHeader {
 constexpr unsigned int kWsMagic = 0x31766b70u;
 constexpr size_t kWsHeaderBytes = 256;
 constexpr int kMaxPersistentSeqs = 4096;      // sequence tables kept in shared memory
+constexpr size_t kMaxSmemPerCta = 227 * 1024;
 
 enum : int { kMetaFirst = 1, kMetaLast = 2, kMetaStop = 4 };
 
@@ -444,7 +457,7 @@ __device__ __forceinline__ void block_prefix_sum(int *v, int n) {
 }
 
 template <int D, int G, typename T>
-__global__ void __launch_bounds__(kThreads, 2) paged_attention_persistent_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(kThreads, PKV_PERSISTENT_CTAS_PER_SM) paged_attention_persistent_kernel(const AttnArgs a) {
     using Gm = Geometry<D>;
     using L = PLayout<D, G, T>;
     constexpr int NSTAGE = Gm::NSTAGE, SE = Gm::STAGE_ELEMS, LPR = Gm::LPR, W = kConsumerWarps;
@@ -796,20 +809,20 @@ __global__ void workspace_init_kernel(WsHeader *h) {
 }
 
 template <int D, int G, typename T> cudaError_t launch_attention(const AttnArgs &a, dim3 grid, cudaStream_t st) {
-    if (a.num_seqs <= kMaxPersistentSeqs) {
-        static bool configured_p = false;    // per template instance; harmless if repeated
+    const size_t psmem = PLayout<D, G, T>::bytes(a.num_seqs);
+    if (a.num_seqs <= kMaxPersistentSeqs && psmem <= kMaxSmemPerCta) {
+        static size_t configured_p = 0;      // largest size set so far for this instance
         auto kern = paged_attention_persistent_kernel<D, G, T>;
-        if (!configured_p) {
-            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)PLayout<D, G, T>::bytes(kMaxPersistentSeqs));
+        if (psmem > configured_p) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
             if (e != cudaSuccess) return e;
-            configured_p = true;
+            configured_p = psmem;
         }
         // enough CTAs to fill the GPU, never more than there can be items
         const long long items = (long long)grid.x * grid.y * grid.z;
-        long long ctas = (long long)sm_count() * 2;
+        long long ctas = (long long)sm_count() * PKV_PERSISTENT_CTAS_PER_SM;
         if (ctas > items) ctas = items;
-        return launch(kern, dim3((unsigned)ctas), dim3(kThreads), PLayout<D, G, T>::bytes(a.num_seqs), st, a);
+        return launch(kern, dim3((unsigned)ctas), dim3(kThreads), psmem, st, a);
     }
     static bool configured = false;
     auto kern = paged_attention_kernel<D, G, T>;
