@@ -43,7 +43,7 @@ namespace {
 #define PKV_SLOTS_PER_WARP_D64 2
 #endif
 #ifndef PKV_PERSISTENT_CTAS_PER_SM
-#define PKV_PERSISTENT_CTAS_PER_SM 2
+#define PKV_PERSISTENT_CTAS_PER_SM 3
 #endif
 
 constexpr int kConsumerWarps = 4;
@@ -67,6 +67,9 @@ template <int D> struct Geometry {
 
 // CTAs per SM the register budget is sized for (shared memory allows 3).
 template <int G> constexpr int min_ctas() { return G >= 4 ? 2 : 3; }
+// Resident CTAs per SM of the persistent kernel (four query heads need the
+// registers of two).
+template <int G> constexpr int persistent_ctas() { return G >= 4 ? 2 : PKV_PERSISTENT_CTAS_PER_SM; }
 
 template <int D, typename T> constexpr size_t smem_bytes() {
     using Gm = Geometry<D>;
@@ -456,8 +459,43 @@ __device__ __forceinline__ void block_prefix_sum(int *v, int n) {
     __syncthreads();
 }
 
+// A work item as the producer sees it.  ent holds, on lane j, block-table
+// entry win + j of the item's sequence (-1 past its blocks).
+struct Item {
+    int s, part, nparts, g, h0, tok0, ntok, nst, npad, nblk, win, ent;
+};
+
+// Ticket t -> item: t / tiles indexes the partitions of all sequences in
+// order (pref holds their prefix sums), t % tiles the query-head tile.
+template <int G>
+__device__ __forceinline__ void decode_item(const AttnArgs &a, const int *pref, const int *ctxs, int S, int tiles,
+                                            unsigned int t, int lane, Item &it) {
+    const int pidx = (int)(t / (unsigned int)tiles);
+    const int tile = (int)(t % (unsigned int)tiles);
+    int lo = 0, hi = S;                                            // pref[lo] <= pidx < pref[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (pref[mid] <= pidx) lo = mid; else hi = mid;
+    }
+    it.s = lo;
+    it.part = pidx - pref[lo];
+    it.nparts = pref[lo + 1] - pref[lo];
+    it.g = tile / a.head_tiles;
+    it.h0 = it.g * (a.head_tiles * G) + (tile % a.head_tiles) * G;
+    const int ctx = ctxs[lo];
+    it.tok0 = it.part * a.partition;
+    int ntok = ctx - it.tok0 < a.partition ? ctx - it.tok0 : a.partition;
+    it.ntok = ntok < 0 ? 0 : ntok;
+    it.nst = (it.ntok + kStageRows - 1) / kStageRows;
+    it.npad = ((it.nst > 0 ? it.nst : 1) + kConsumerWarps - 1) / kConsumerWarps * kConsumerWarps;
+    it.nblk = (ctx + (1 << a.log2_block) - 1) >> a.log2_block;
+    it.win = it.tok0 >> a.log2_block;
+    const int j = it.win + lane;
+    it.ent = j < it.nblk ? __ldg(a.tables + (size_t)lo * a.max_blocks + j) : -1;
+}
+
 template <int D, int G, typename T>
-__global__ void __launch_bounds__(kThreads, PKV_PERSISTENT_CTAS_PER_SM) paged_attention_persistent_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(kThreads, persistent_ctas<G>()) paged_attention_persistent_kernel(const AttnArgs a) {
     using Gm = Geometry<D>;
     using L = PLayout<D, G, T>;
     constexpr int NSTAGE = Gm::NSTAGE, SE = Gm::STAGE_ELEMS, LPR = Gm::LPR, W = kConsumerWarps;
@@ -519,38 +557,30 @@ __global__ void __launch_bounds__(kThreads, PKV_PERSISTENT_CTAS_PER_SM) paged_at
         const uint32_t copy_bytes = (uint32_t)(rows_per_copy * D * sizeof(T));
         const uint32_t q_bytes = (uint32_t)(G * D * sizeof(T));
         const uint64_t policy = policy_evict_first();
-        unsigned int ticket = 0;
-        if (lane == 0) ticket = atomicAdd(&hdr->next, 1u);
-        ticket = __shfl_sync(kFull, ticket, 0);
+        // Tickets: the first item of CTA c is item c; later ones come from the
+        // counter, offset by the grid size.  The next item is decoded (and its
+        // first 32 block-table entries loaded) one item ahead, so the producer
+        // does not wait on the table at item boundaries.
+        unsigned int cur_t = blockIdx.x;
+        unsigned int nxt_raw = 0;
+        if (lane == 0) nxt_raw = gridDim.x + atomicAdd(&hdr->next, 1u);
+        Item cur, nx;
+        if (cur_t < N) decode_item<G>(a, pref, ctxs, S, tiles, cur_t, lane, cur);
         int kk = 0, items = 0;
         bool dead = false;
-        while (ticket < N && !dead) {
-            unsigned int nxt = 0;
-            if (lane == 0) nxt = atomicAdd(&hdr->next, 1u);      // the next item's ticket, used below
-            const int pidx = (int)(ticket / (unsigned int)tiles);
-            const int tile = (int)(ticket % (unsigned int)tiles);
-            int lo = 0, hi = S;                                    // pref[lo] <= pidx < pref[hi]
-            while (hi - lo > 1) {
-                const int mid = (lo + hi) >> 1;
-                if (pref[mid] <= pidx) lo = mid; else hi = mid;
-            }
-            const int s = lo, part = pidx - pref[s], nparts = pref[s + 1] - pref[s];
-            const int g = tile / a.head_tiles;
-            const int h0 = g * (a.head_tiles * G) + (tile % a.head_tiles) * G;
-            const int ctx = ctxs[s];
-            const int tok0 = part * a.partition;
-            int ntok = ctx - tok0 < a.partition ? ctx - tok0 : a.partition;
-            if (ntok < 0) ntok = 0;
-            const int nst = (ntok + kStageRows - 1) / kStageRows;
-            const int npad = ((nst > 0 ? nst : 1) + W - 1) / W * W;
+        while (cur_t < N && !dead) {
+            const unsigned int nxt_t = __shfl_sync(kFull, nxt_raw, 0);
+            if (nxt_t < N) decode_item<G>(a, pref, ctxs, S, tiles, nxt_t, lane, nx);
+            if (lane == 0) nxt_raw = gridDim.x + atomicAdd(&hdr->next, 1u);
+            const int s = cur.s, part = cur.part, nparts = cur.nparts, g = cur.g, h0 = cur.h0;
+            const int tok0 = cur.tok0, ntok = cur.ntok, nst = cur.nst, npad = cur.npad, nblk = cur.nblk;
             const int32_t *trow = a.tables + (size_t)s * a.max_blocks;
-            const int nblk = (ctx + B - 1) >> a.log2_block;
             // Query buffer: written with the item's first W stages; with NQ =
             // NSTAGE / W buffers and every item at least W stages long, a
             // buffer is rewritten only after its previous item's first stages
             // have been consumed.
             const int qb = items % NQ;
-            int win = -(1 << 30), ent = -1;
+            int win = cur.win, ent = cur.ent;
             for (int i = 0; i < npad; i++, kk++) {
                 int e[8];
                 int off0 = 0;
@@ -566,14 +596,16 @@ __global__ void __launch_bounds__(kThreads, PKV_PERSISTENT_CTAS_PER_SM) paged_at
 #pragma unroll
                     for (int j = 0; j < 8; j++) e[j] = __shfl_sync(kFull, ent, (lb0 + j - win) & 31);
                 }
+                const int slot = kk % NSTAGE;
+                const bool withq = i < W && i < nst;               // warp i's first stage of the item
+                int ncopies = 0;
                 if (lane == 0) {
-                    const int slot = kk % NSTAGE;
                     if (kk >= NSTAGE && !mbar_wait(&empty[slot], ((kk / NSTAGE) - 1) & 1, kWaitLimitCycles)) {
                         latch(a.st, kFlagTimeout, kk);
                         dead = true;
                     }
                     if (!dead) {
-                        int nv = 0, ncopies = 0;
+                        int nv = 0;
                         if (i < nst) {
                             nv = ntok - i * kStageRows < kStageRows ? ntok - i * kStageRows : kStageRows;
                             for (int j = 0; j < cps && j < 8; j++) {
@@ -587,7 +619,6 @@ __global__ void __launch_bounds__(kThreads, PKV_PERSISTENT_CTAS_PER_SM) paged_at
                                 ncopies = j + 1;
                             }
                         }
-                        const bool withq = i < W && i < nst;       // warp i's first stage of the item
                         StageMeta &m = meta[slot];
                         m.s = s;
                         m.h0 = h0;
@@ -597,22 +628,30 @@ __global__ void __launch_bounds__(kThreads, PKV_PERSISTENT_CTAS_PER_SM) paged_at
                         m.qbuf = qb;
                         m.flags = (i < W ? kMetaFirst : 0) | (i >= npad - W ? kMetaLast : 0);
                         mbar_arrive_expect_tx(&full[slot], 2u * copy_bytes * (uint32_t)ncopies + (withq ? q_bytes : 0u));
-                        if (withq)
-                            bulk_g2s(qs + (size_t)(qb * W + i) * G * D, qg + ((size_t)s * a.num_heads + h0) * D,
-                                     q_bytes, &full[slot]);
-                        for (int j = 0; j < ncopies; j++) {
-                            const size_t goff = (((size_t)e[j] * a.num_kv_heads + g) * B + off0) * D;
-                            T *dk = ring + (size_t)(slot * 2) * SE + (size_t)j * rows_per_copy * D;
-                            bulk_g2s_hint(dk, kc + goff, copy_bytes, &full[slot], policy);
-                            bulk_g2s_hint(dk + SE, vc + goff, copy_bytes, &full[slot], policy);
-                        }
                     }
                 }
                 dead = __shfl_sync(kFull, dead ? 1 : 0, 0) != 0;
                 if (dead) break;
+                ncopies = __shfl_sync(kFull, ncopies, 0);
+                // one bulk copy per lane: lane 2j moves block j's K tile, lane 2j+1 its V tile,
+                // lane 2 * ncopies the item's query heads
+                if (lane < 2 * ncopies) {
+                    const int j = lane >> 1;
+                    int pj = e[0];
+#pragma unroll
+                    for (int x = 1; x < 8; x++)
+                        if (x == j) pj = e[x];
+                    const size_t goff = (((size_t)pj * a.num_kv_heads + g) * B + off0) * D;
+                    T *dst = ring + (size_t)(slot * 2 + (lane & 1)) * SE + (size_t)j * rows_per_copy * D;
+                    bulk_g2s_hint(dst, ((lane & 1) ? vc : kc) + goff, copy_bytes, &full[slot], policy);
+                } else if (withq && lane == 2 * ncopies) {
+                    bulk_g2s(qs + (size_t)(qb * W + i) * G * D, qg + ((size_t)s * a.num_heads + h0) * D, q_bytes,
+                             &full[slot]);
+                }
             }
             items++;
-            ticket = __shfl_sync(kFull, nxt, 0);
+            cur_t = nxt_t;
+            cur = nx;
         }
         if (lane == 0) {
             // one stop mark per consumer warp
@@ -820,7 +859,7 @@ template <int D, int G, typename T> cudaError_t launch_attention(const AttnArgs 
         }
         // enough CTAs to fill the GPU, never more than there can be items
         const long long items = (long long)grid.x * grid.y * grid.z;
-        long long ctas = (long long)sm_count() * PKV_PERSISTENT_CTAS_PER_SM;
+        long long ctas = (long long)sm_count() * persistent_ctas<G>();
         if (ctas > items) ctas = items;
         return launch(kern, dim3((unsigned)ctas), dim3(kThreads), psmem, st, a);
     }

@@ -16,8 +16,12 @@ from typing import Optional, Sequence
 import numpy as np
 import torch
 
-from . import (BlockAllocator, copy_blocks, kv_reshape_and_cache, make_workspace, paged_attention_decode,
-               paged_attention_workspace_size)
+import ctypes
+import math
+
+from . import (BlockAllocator, PkvError, copy_blocks, kv_reshape_and_cache, make_workspace,
+               paged_attention_decode, paged_attention_workspace_size)
+from ._lib import load
 
 
 @dataclasses.dataclass
@@ -126,3 +130,64 @@ class PagedKVCache:
         self.copy_on_write(step.pairs)
         self.write(key, value, step.slots)
         return self.attend(query, step, out, scale, partition_size)
+
+    def prepare(self, query: torch.Tensor, key: torch.Tensor, value: torch.Tensor, step: DeviceStep,
+                out: torch.Tensor, scale: Optional[float] = None, partition_size: int = 0,
+                stream: Optional[torch.cuda.Stream] = None) -> "PreparedStep":
+        """The device calls of a decode step on fixed buffers, with their C-ABI
+        arguments built once."""
+        return PreparedStep(self, query, key, value, step, out, scale, partition_size, stream)
+
+
+class PreparedStep:
+    """copy_blocks, kv_reshape_and_cache and paged_attention_decode for one
+    set of buffers, their arguments checked and marshalled once: issuing the
+    step then costs three or four plain C calls.  For decode loops that run
+    the same buffers every iteration (the buffers' contents may change)."""
+
+    def __init__(self, eng: PagedKVCache, query, key, value, step: DeviceStep, out, scale, partition_size, stream):
+        self._L = load()
+        S, H, d = query.shape
+        assert out.shape == query.shape and out.dtype == query.dtype == eng.key_cache.dtype
+        assert key.shape == value.shape == (step.slots.shape[0], eng.num_kv_heads, d)
+        for t in (query, key, value, out, step.slots, step.tables, step.context_lens, step.pairs):
+            assert t.is_cuda and t.is_contiguous()
+        code = 1 if query.dtype == torch.bfloat16 else 0
+        st = ctypes.c_void_p((stream or torch.cuda.current_stream(eng.device)).cuda_stream)
+        ws = eng.workspace(S, H, step.max_context_len, partition_size)
+        self._keep = (query, key, value, step, out, ws)
+        NB, B = eng.num_blocks, eng.block_size
+        block_bytes = eng.num_kv_heads * B * d * eng.key_cache.element_size()
+        n = step.pairs.shape[0] if step.pairs.dim() == 2 else 0
+        self._copy = [(c.data_ptr(), step.pairs.data_ptr(), n, block_bytes, NB, st)
+                      for c in (eng.key_cache, eng.value_cache)] if n else []
+        T = step.slots.shape[0]
+        self._write = (key.data_ptr(), value.data_ptr(), eng.key_cache.data_ptr(), eng.value_cache.data_ptr(),
+                       step.slots.data_ptr(), T, eng.num_kv_heads, d, B, NB, code, st)
+        self._attend = (out.data_ptr(), query.data_ptr(), eng.key_cache.data_ptr(), eng.value_cache.data_ptr(),
+                        step.tables.data_ptr(), step.context_lens.data_ptr(), S, step.tables.shape[1],
+                        step.max_context_len, B, NB, H, eng.num_kv_heads, d,
+                        float(1.0 / math.sqrt(d) if scale is None else scale), partition_size, ws.data_ptr(),
+                        ws.numel(), code, st)
+
+    def copy(self) -> None:
+        for args in self._copy:
+            rc = self._L.copy_blocks(*args)
+            if rc:
+                raise PkvError(rc, "copy_blocks")
+
+    def write(self) -> None:
+        if self._write[5]:
+            rc = self._L.kv_reshape_and_cache(*self._write)
+            if rc:
+                raise PkvError(rc, "kv_reshape_and_cache")
+
+    def attend(self) -> None:
+        rc = self._L.paged_attention_decode(*self._attend)
+        if rc:
+            raise PkvError(rc, "paged_attention_decode")
+
+    def __call__(self) -> None:
+        self.copy()
+        self.write()
+        self.attend()

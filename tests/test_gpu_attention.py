@@ -242,3 +242,17 @@ def test_launch_count_and_native_library(cuda_device):
     import os
     maps = open("/proc/self/maps").read()
     assert os.path.realpath(pkv.library_path()) in maps
+
+
+def test_prepared_step_matches_decode(cuda_device):
+    """The prepared decode step (arguments marshalled once) launches the same
+    calls as the engine's decode."""
+    w = _custom(H=8, Hkv=4, ctx=(300, 1, 1200), S=3)
+    c = Case(w, cuda_device, partition_size=256)
+    out = torch.empty_like(c.q_dev)
+    prep = c.eng.prepare(c.q_dev, c.k_dev, c.v_dev, c.dev, out, partition_size=256)
+    before = pkv.launch_count()
+    prep()
+    pkv.check()
+    assert pkv.launch_count() - before == 3
+    assert torch.equal(out, c.out)
