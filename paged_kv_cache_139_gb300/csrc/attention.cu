@@ -27,7 +27,13 @@
 //     the four warps' states are merged through shared memory.
 //   * All mbarrier waits are bounded; a wait that gives up latches a timeout
 //     in the status word and the kernel drains its copies and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <cfloat>
+#include <cstring>
+#include <mutex>
+#include <type_traits>
 
 #include "pkv_host.cuh"
 
@@ -157,6 +163,128 @@ __device__ __forceinline__ void consume_stage(const T *Ks, const T *Vs, int nval
             const float w = __shfl_sync(kFull, p[h], r * LPR + i);
 #pragma unroll
             for (int e = 0; e < 8; e++) acc[h][e] = fmaf(w, vf[e], acc[h][e]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Tensor-core stage for query-head groups (GQA): the G heads of one kv head
+// form the rows of a 16 x d query tile, so QK^T and PV become m16n8k16 MMAs
+// (fp32 accumulation).  The K and V tiles come from tiled TMA copies with the
+// 128-byte swizzle: a tile is [d/64 halves][32 tokens][64 elements], and the
+// 16-byte chunk c of row r sits at chunk c ^ (r % 8), which keeps ldmatrix
+// free of bank conflicts.
+// ---------------------------------------------------------------------------
+
+// Element offset of 16-byte chunk `chunk` (0 .. d/8-1) of token row `row`.
+__device__ __forceinline__ int swz(int row, int chunk) {
+    return (chunk >> 3) * (kStageRows * 64) + row * 64 + (((chunk & 7) ^ (row & 7)) << 3);
+}
+
+template <int D> struct MmaState {
+    static constexpr int NT = D / 8;   // 8-wide column tiles of the output
+    float o[NT][4];                    // rows lane/4 (c0, c1) and lane/4 + 8 (c2, c3, unused)
+    float m;                           // running max of row lane/4 (log2 domain)
+    float l;                           // this lane's share of the row's sum of exponentials
+};
+
+template <int D> __device__ __forceinline__ void mma_reset(MmaState<D> &st) {
+#pragma unroll
+    for (int n = 0; n < MmaState<D>::NT; n++)
+#pragma unroll
+        for (int e = 0; e < 4; e++) st.o[n][e] = 0.f;
+    st.m = -INFINITY;
+    st.l = 0.f;
+}
+
+// qa[ks] = (a0, a2) of k-step ks: query row lane/4 (zero past G heads);
+// rows 8-15 of the tile (a1, a3) are zero.
+template <int D, int G, typename T>
+__device__ __forceinline__ void mma_load_q(uint32_t (&qa)[D / 16][2], const T *q, int lane) {
+    const int row = lane >> 2, cq = lane & 3;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ks++) {
+        if (row < G) {
+            qa[ks][0] = *reinterpret_cast<const uint32_t *>(q + row * D + ks * 16 + cq * 2);
+            qa[ks][1] = *reinterpret_cast<const uint32_t *>(q + row * D + ks * 16 + 8 + cq * 2);
+        } else {
+            qa[ks][0] = qa[ks][1] = 0u;
+        }
+    }
+}
+
+template <int D, typename T, bool FULL_STAGE>
+__device__ __forceinline__ void consume_stage_mma(const T *Ks, T *Vs, int nvalid, int lane,
+                                                  const uint32_t (&qa)[D / 16][2], MmaState<D> &st,
+                                                  float scale_log2) {
+    constexpr int NT = D / 8;
+    const int cq = lane & 3;
+    if (!FULL_STAGE) {
+        // rows past the context may hold anything: zero them in V (0 * NaN would poison PV)
+        for (int r = nvalid; r < kStageRows; r++)
+            for (int e = lane * 8; e < D; e += 32 * 8)
+                *reinterpret_cast<uint4 *>(Vs + (e >> 6) * (kStageRows * 64) + r * 64 + (e & 63)) =
+                    make_uint4(0u, 0u, 0u, 0u);
+        __syncwarp();
+    }
+    // S = Q K^T: 4 column tiles of 8 tokens
+    float s[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 4; nt++)
+#pragma unroll
+        for (int e = 0; e < 4; e++) s[nt][e] = 0.f;
+#pragma unroll
+    for (int kp = 0; kp < D / 32; kp++) {
+#pragma unroll
+        for (int nt = 0; nt < 4; nt++) {
+            uint32_t b[4];
+            ldmatrix_x4(b, Ks + swz(nt * 8 + (lane & 7), kp * 4 + (lane >> 3)));
+            const uint32_t a0[4] = {qa[2 * kp][0], 0u, qa[2 * kp][1], 0u};
+            const uint32_t a1[4] = {qa[2 * kp + 1][0], 0u, qa[2 * kp + 1][1], 0u};
+            Mma<T>::run(s[nt], a0, b[0], b[1]);
+            Mma<T>::run(s[nt], a1, b[2], b[3]);
+        }
+    }
+    // online softmax over the row's 8 tokens on this lane (a quad holds the row)
+    float x[8];
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        x[j] = s[j >> 1][j & 1] * scale_log2;
+        if (!FULL_STAGE && (j >> 1) * 8 + cq * 2 + (j & 1) >= nvalid) x[j] = -INFINITY;
+    }
+    float mx = x[0];
+#pragma unroll
+    for (int j = 1; j < 8; j++) mx = fmaxf(mx, x[j]);
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+    const float mnew = fmaxf(st.m, mx);
+    const float alpha = exp2f(st.m - mnew);
+    float p[8], psum = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        p[j] = exp2f(x[j] - mnew);
+        psum += p[j];
+    }
+    st.l = st.l * alpha + psum;
+    st.m = mnew;
+#pragma unroll
+    for (int n = 0; n < NT; n++) {
+        st.o[n][0] *= alpha;
+        st.o[n][1] *= alpha;
+    }
+    // O += P V: the S accumulators of two column tiles are the A fragment of one k-step
+#pragma unroll
+    for (int kt = 0; kt < 2; kt++) {
+        const uint32_t pa[4] = {Mma<T>::pack(p[4 * kt], p[4 * kt + 1]), 0u, Mma<T>::pack(p[4 * kt + 2], p[4 * kt + 3]),
+                                0u};
+        const int mi = lane >> 3;
+        const int tok = kt * 16 + (mi & 1) * 8 + (lane & 7);
+#pragma unroll
+        for (int np = 0; np < NT / 2; np++) {
+            uint32_t b[4];
+            ldmatrix_x4_trans(b, Vs + swz(tok, 2 * np + (mi >> 1)));
+            Mma<T>::run(st.o[2 * np], pa, b[0], b[1]);
+            Mma<T>::run(st.o[2 * np + 1], pa, b[2], b[3]);
         }
     }
 }
@@ -428,7 +556,8 @@ template <int D, int G, typename T> struct PLayout {
     static constexpr size_t bars = merge + (size_t)2 * kConsumerWarps * G * (D + 2) * sizeof(float);
     static constexpr size_t meta = bars + (size_t)(2 * Gm::NSTAGE + 2) * sizeof(uint64_t);
     static constexpr size_t seqs = meta + (size_t)Gm::NSTAGE * sizeof(StageMeta);
-    static size_t bytes(int S) { return seqs + (size_t)(2 * S + 1) * sizeof(int); }
+    // + 1024: the kernel moves its base up to the next 1024-byte boundary
+    static size_t bytes(int S) { return seqs + (size_t)(2 * S + 1) * sizeof(int) + 1024; }
 };
 
 // In place: v[1..n] := inclusive prefix sums of v[1..n]; v[0] := 0.
@@ -494,13 +623,20 @@ __device__ __forceinline__ void decode_item(const AttnArgs &a, const int *pref, 
     it.ent = j < it.nblk ? __ldg(a.tables + (size_t)lo * a.max_blocks + j) : -1;
 }
 
-template <int D, int G, typename T>
-__global__ void __launch_bounds__(kThreads, persistent_ctas<G>()) paged_attention_persistent_kernel(const AttnArgs a) {
+// MMA selects the tensor-core stage (query-head groups of 4 or 8) fed by
+// tiled TMA copies through tmk / tmv; otherwise the CUDA-core stage fed by
+// 1-D bulk copies (tmk / tmv unused).
+template <int D, int G, typename T, bool MMA>
+__global__ void __launch_bounds__(kThreads, persistent_ctas<G>())
+    paged_attention_persistent_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmk,
+                                      const __grid_constant__ CUtensorMap tmv) {
     using Gm = Geometry<D>;
     using L = PLayout<D, G, T>;
     constexpr int NSTAGE = Gm::NSTAGE, SE = Gm::STAGE_ELEMS, LPR = Gm::LPR, W = kConsumerWarps;
     constexpr int NQ = L::NQ;
-    extern __shared__ __align__(128) unsigned char smem[];
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // the 128-byte swizzle repeats every 1024 bytes: the ring starts on such a boundary
+    unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     T *ring = reinterpret_cast<T *>(smem + L::ring);                 // [NSTAGE][2][32][D]
     T *qs = reinterpret_cast<T *>(smem + L::qs);                     // [NQ][W][G][D]
     float *mg = reinterpret_cast<float *>(smem + L::merge);          // [2][W][G][D + 2]: o, m, l
@@ -633,9 +769,26 @@ __global__ void __launch_bounds__(kThreads, persistent_ctas<G>()) paged_attentio
                 dead = __shfl_sync(kFull, dead ? 1 : 0, 0) != 0;
                 if (dead) break;
                 ncopies = __shfl_sync(kFull, ncopies, 0);
-                // one bulk copy per lane: lane 2j moves block j's K tile, lane 2j+1 its V tile,
-                // lane 2 * ncopies the item's query heads
-                if (lane < 2 * ncopies) {
+                if (MMA) {
+                    // one tiled copy per lane: lane (2j + h) * 2 + t moves half h (64 elements of d)
+                    // of block j's K (t = 0) or V (t = 1) tile; lane 0 also moves the query heads
+                    constexpr int HALVES = D / 64;
+                    if (lane < ncopies * HALVES * 2) {
+                        const int t = lane & 1, h = (lane >> 1) % HALVES, j = (lane >> 1) / HALVES;
+                        int pj = e[0];
+#pragma unroll
+                        for (int x = 1; x < 8; x++)
+                            if (x == j) pj = e[x];
+                        T *dst = ring + (size_t)(slot * 2 + t) * SE + h * (kStageRows * 64) + j * rows_per_copy * 64;
+                        tma_load_4d(dst, t ? (const void *)&tmv : (const void *)&tmk, h * 64, off0, g, pj, &full[slot],
+                                    policy);
+                    }
+                    if (withq && lane == 0)
+                        bulk_g2s(qs + (size_t)(qb * W + i) * G * D, qg + ((size_t)s * a.num_heads + h0) * D, q_bytes,
+                                 &full[slot]);
+                } else if (lane < 2 * ncopies) {
+                    // one bulk copy per lane: lane 2j moves block j's K tile, lane 2j+1 its V tile,
+                    // lane 2 * ncopies the item's query heads
                     const int j = lane >> 1;
                     int pj = e[0];
 #pragma unroll
@@ -644,7 +797,7 @@ __global__ void __launch_bounds__(kThreads, persistent_ctas<G>()) paged_attentio
                     const size_t goff = (((size_t)pj * a.num_kv_heads + g) * B + off0) * D;
                     T *dst = ring + (size_t)(slot * 2 + (lane & 1)) * SE + (size_t)j * rows_per_copy * D;
                     bulk_g2s_hint(dst, ((lane & 1) ? vc : kc) + goff, copy_bytes, &full[slot], policy);
-                } else if (withq && lane == 2 * ncopies) {
+                } else if (!MMA && withq && lane == 2 * ncopies) {
                     bulk_g2s(qs + (size_t)(qb * W + i) * G * D, qg + ((size_t)s * a.num_heads + h0) * D, q_bytes,
                              &full[slot]);
                 }
@@ -678,14 +831,23 @@ __global__ void __launch_bounds__(kThreads, persistent_ctas<G>()) paged_attentio
 
     // ---------------- consumers ----------------
     const int r = lane / LPR, c = lane % LPR;
-    float qf[G][8], m[G], lsum[G], acc[G][8];
+    float qf[G][8], m[G], lsum[G], acc[G][8];          // CUDA-core stage state
+    uint32_t qa[D / 16][2];                            // tensor-core stage state
+    MmaState<D> ms;
+    auto reset = [&]() {
+        if constexpr (MMA) {
+            mma_reset(ms);
+        } else {
 #pragma unroll
-    for (int h = 0; h < G; h++) {
-        m[h] = -INFINITY;
-        lsum[h] = 0.f;
+            for (int h = 0; h < G; h++) {
+                m[h] = -INFINITY;
+                lsum[h] = 0.f;
 #pragma unroll
-        for (int e = 0; e < 8; e++) acc[h][e] = 0.f;
-    }
+                for (int e = 0; e < 8; e++) acc[h][e] = 0.f;
+            }
+        }
+    };
+    reset();
     int jitem = 0;
     for (int k = warp;; k += W) {
         const int slot = k % NSTAGE;
@@ -700,48 +862,76 @@ __global__ void __launch_bounds__(kThreads, persistent_ctas<G>()) paged_attentio
             if (lane == 0) mbar_arrive(&empty[slot]);
             break;
         }
-        if ((md.flags & kMetaFirst) && md.nvalid > 0) {
-            const T *qp = qs + (size_t)(md.qbuf * W + warp) * G * D + c * 8;
-#pragma unroll
-            for (int h = 0; h < G; h++) {
-                const uint4 raw = *reinterpret_cast<const uint4 *>(qp + h * D);
-                F16Traits<T>::to_f32(raw, qf[h]);
-#pragma unroll
-                for (int e = 0; e < 8; e++) qf[h][e] *= a.scale_log2;
+        const T *qp = qs + (size_t)(md.qbuf * W + warp) * G * D;
+        T *Ks = ring + (size_t)(slot * 2) * SE;
+        if constexpr (MMA) {
+            if ((md.flags & kMetaFirst) && md.nvalid > 0) mma_load_q<D, G, T>(qa, qp, lane);
+            if (md.nvalid == kStageRows) {
+                consume_stage_mma<D, T, true>(Ks, Ks + SE, md.nvalid, lane, qa, ms, a.scale_log2);
+            } else if (md.nvalid > 0) {
+                consume_stage_mma<D, T, false>(Ks, Ks + SE, md.nvalid, lane, qa, ms, a.scale_log2);
+                fence_proxy_async_smem();        // the zeroed rows, before TMA refills the slot
             }
+        } else {
+            if ((md.flags & kMetaFirst) && md.nvalid > 0) {
+#pragma unroll
+                for (int h = 0; h < G; h++) {
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(qp + h * D + c * 8);
+                    F16Traits<T>::to_f32(raw, qf[h]);
+#pragma unroll
+                    for (int e = 0; e < 8; e++) qf[h][e] *= a.scale_log2;
+                }
+            }
+            if (md.nvalid == kStageRows)
+                consume_stage<D, G, T, true>(Ks, Ks + SE, md.nvalid, r, c, qf, m, lsum, acc);
+            else if (md.nvalid > 0)
+                consume_stage<D, G, T, false>(Ks, Ks + SE, md.nvalid, r, c, qf, m, lsum, acc);
         }
-        const T *Ks = ring + (size_t)(slot * 2) * SE;
-        if (md.nvalid == kStageRows)
-            consume_stage<D, G, T, true>(Ks, Ks + SE, md.nvalid, r, c, qf, m, lsum, acc);
-        else if (md.nvalid > 0)
-            consume_stage<D, G, T, false>(Ks, Ks + SE, md.nvalid, r, c, qf, m, lsum, acc);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
         if (!(md.flags & kMetaLast)) continue;
 
         // ---- the item's merge: this warp's state into buffer b, then W-way combine ----
         const int b = jitem & 1;
-#pragma unroll
-        for (int h = 0; h < G; h++) {
-            lsum[h] = warp_sum(lsum[h]);
-#pragma unroll
-            for (int e = 0; e < 8; e++) {
-#pragma unroll
-                for (int o = LPR; o < 32; o <<= 1) acc[h][e] += __shfl_xor_sync(kFull, acc[h][e], o);
-            }
-        }
         float *mw = mg + (size_t)(b * W + warp) * G * (D + 2);
-        if (r == 0) {
+        if constexpr (MMA) {
+            ms.l += __shfl_xor_sync(kFull, ms.l, 1);
+            ms.l += __shfl_xor_sync(kFull, ms.l, 2);
+            const int row = lane >> 2, cq = lane & 3;
+            if (row < G) {
+                float *mr = mw + row * (D + 2);
 #pragma unroll
-            for (int h = 0; h < G; h++)
-#pragma unroll
-                for (int e = 0; e < 8; e++) mw[h * (D + 2) + c * 8 + e] = acc[h][e];
-        }
-        if (lane == 0) {
+                for (int n = 0; n < D / 8; n++) {
+                    mr[n * 8 + cq * 2] = ms.o[n][0];
+                    mr[n * 8 + cq * 2 + 1] = ms.o[n][1];
+                }
+                if (cq == 0) {
+                    mr[D] = ms.m;
+                    mr[D + 1] = ms.l;
+                }
+            }
+        } else {
 #pragma unroll
             for (int h = 0; h < G; h++) {
-                mw[h * (D + 2) + D] = m[h];
-                mw[h * (D + 2) + D + 1] = lsum[h];
+                lsum[h] = warp_sum(lsum[h]);
+#pragma unroll
+                for (int e = 0; e < 8; e++) {
+#pragma unroll
+                    for (int o = LPR; o < 32; o <<= 1) acc[h][e] += __shfl_xor_sync(kFull, acc[h][e], o);
+                }
+            }
+            if (r == 0) {
+#pragma unroll
+                for (int h = 0; h < G; h++)
+#pragma unroll
+                    for (int e = 0; e < 8; e++) mw[h * (D + 2) + c * 8 + e] = acc[h][e];
+            }
+            if (lane == 0) {
+#pragma unroll
+                for (int h = 0; h < G; h++) {
+                    mw[h * (D + 2) + D] = m[h];
+                    mw[h * (D + 2) + D + 1] = lsum[h];
+                }
             }
         }
         mbar_arrive(&mbar[b]);                                   // every lane, after its own writes
@@ -776,13 +966,7 @@ __global__ void __launch_bounds__(kThreads, persistent_ctas<G>()) paged_attentio
             }
         }
         jitem++;
-#pragma unroll
-        for (int h = 0; h < G; h++) {
-            m[h] = -INFINITY;
-            lsum[h] = 0.f;
-#pragma unroll
-            for (int e = 0; e < 8; e++) acc[h][e] = 0.f;
-        }
+        reset();
     }
 }
 
@@ -847,11 +1031,66 @@ __global__ void workspace_init_kernel(WsHeader *h) {
     h->magic = kWsMagic;
 }
 
+// cuTensorMapEncodeTiled from the driver, looked up once.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// The cache [NB][Hkv][B][D] as a 4-D tensor (innermost first); a box is 64
+// elements of d by min(B, 32) tokens of one (block, kv head), 128-byte swizzle.
+bool encode_cache_map(CUtensorMap *map, const void *base, int num_blocks, int Hkv, int B, int D, bool bf16) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)B, (cuuint64_t)Hkv, (cuuint64_t)(num_blocks > 0 ? num_blocks : 1)};
+    const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)B * D * 2, (cuuint64_t)Hkv * B * D * 2};
+    const cuuint32_t box[4] = {64u, (cuuint32_t)(B < kStageRows ? B : kStageRows), 1u, 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    return enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+               const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, int G, typename T, bool MMA>
+cudaError_t launch_persistent(const AttnArgs &a, dim3 grid, cudaStream_t st) {
+    const size_t psmem = PLayout<D, G, T>::bytes(a.num_seqs);
+    static size_t configured_p = 0;          // largest size set so far for this instance
+    auto kern = paged_attention_persistent_kernel<D, G, T, MMA>;
+    if (psmem > configured_p) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
+        if (e != cudaSuccess) return e;
+        configured_p = psmem;
+    }
+    CUtensorMap tmk, tmv;
+    std::memset(&tmk, 0, sizeof tmk);
+    std::memset(&tmv, 0, sizeof tmv);
+    if (MMA) {
+        const bool bf16 = sizeof(T) == 2 && std::is_same<T, __nv_bfloat16>::value;
+        if (!encode_cache_map(&tmk, a.k_cache, a.num_blocks, a.num_kv_heads, 1 << a.log2_block, D, bf16) ||
+            !encode_cache_map(&tmv, a.v_cache, a.num_blocks, a.num_kv_heads, 1 << a.log2_block, D, bf16))
+            return cudaErrorInvalidValue;
+    }
+    // enough CTAs to fill the GPU, never more than there can be items
+    const long long items = (long long)grid.x * grid.y * grid.z;
+    long long ctas = (long long)sm_count() * persistent_ctas<G>();
+    if (ctas > items) ctas = items;
+    return launch(kern, dim3((unsigned)ctas), dim3(kThreads), psmem, st, a, tmk, tmv);
+}
+
 template <int D, int G, typename T> cudaError_t launch_attention(const AttnArgs &a, dim3 grid, cudaStream_t st) {
     const size_t psmem = PLayout<D, G, T>::bytes(a.num_seqs);
     if (a.num_seqs <= kMaxPersistentSeqs && psmem <= kMaxSmemPerCta) {
         static size_t configured_p = 0;      // largest size set so far for this instance
-        auto kern = paged_attention_persistent_kernel<D, G, T>;
+        auto kern = paged_attention_persistent_kernel<D, G, T, false>;
         if (psmem > configured_p) {
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
             if (e != cudaSuccess) return e;
@@ -861,7 +1100,9 @@ template <int D, int G, typename T> cudaError_t launch_attention(const AttnArgs 
         const long long items = (long long)grid.x * grid.y * grid.z;
         long long ctas = (long long)sm_count() * persistent_ctas<G>();
         if (ctas > items) ctas = items;
-        return launch(kern, dim3((unsigned)ctas), dim3(kThreads), psmem, st, a);
+        CUtensorMap none;
+        std::memset(&none, 0, sizeof none);
+        return launch(kern, dim3((unsigned)ctas), dim3(kThreads), psmem, st, a, none, none);
     }
     static bool configured = false;
     auto kern = paged_attention_kernel<D, G, T>;
@@ -874,7 +1115,34 @@ template <int D, int G, typename T> cudaError_t launch_attention(const AttnArgs 
     return launch(kern, grid, dim3(kThreads), smem, st, a);
 }
 
+// Query-head tile per CTA item for a group of `group` query heads per kv head:
+// 8 or 4 heads go to the tensor-core stage, 2 or 1 to the CUDA-core stage
+// (the grid kernel, used for very large batches, has the CUDA-core stage
+// only and tiles at most 4 heads).
+int head_tile(int group, bool persistent) {
+    if (persistent && group % 8 == 0) return 8;
+    if (group % 4 == 0) return 4;
+    if (group % 2 == 0) return 2;
+    return 1;
+}
+
+bool use_persistent(int num_seqs, int D, int G, int esize) {
+    (void)esize;
+    if (num_seqs > kMaxPersistentSeqs) return false;
+    size_t need = 0;
+    if (D == 64)
+        need = G == 8 ? PLayout<64, 8, __half>::bytes(num_seqs) : G == 4 ? PLayout<64, 4, __half>::bytes(num_seqs)
+                                                                      : PLayout<64, 2, __half>::bytes(num_seqs);
+    else
+        need = G == 8 ? PLayout<128, 8, __half>::bytes(num_seqs) : G == 4 ? PLayout<128, 4, __half>::bytes(num_seqs)
+                                                                       : PLayout<128, 2, __half>::bytes(num_seqs);
+    return need <= kMaxSmemPerCta;
+}
+
 template <int D, typename T> cudaError_t dispatch_g(int G, const AttnArgs &a, dim3 grid, cudaStream_t st) {
+    const bool persistent = use_persistent(a.num_seqs, D, G, 2);
+    if (persistent && G == 8) return launch_persistent<D, 8, T, true>(a, grid, st);
+    if (persistent && G == 4) return launch_persistent<D, 4, T, true>(a, grid, st);
     switch (G) {
     case 4: return launch_attention<D, 4, T>(a, grid, st);
     case 2: return launch_attention<D, 2, T>(a, grid, st);
@@ -968,7 +1236,8 @@ pkv_status paged_attention_decode(void *out, const void *query, const void *key_
     if (!st) return fail(PKV_ECUDA, "paged_attention_decode: no device status word");
 
     const int group = num_heads / num_kv_heads;
-    const int G = group % 4 == 0 ? 4 : (group % 2 == 0 ? 2 : 1);
+    int G = head_tile(group, true);
+    if (!use_persistent(num_seqs, head_dim, G, 2)) G = head_tile(group, false);
     AttnArgs a;
     a.out = out;
     unsigned char *ws = static_cast<unsigned char *>(workspace);
