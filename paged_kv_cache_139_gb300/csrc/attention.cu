@@ -51,6 +51,17 @@ namespace {
 #ifndef PKV_PERSISTENT_CTAS_PER_SM
 #define PKV_PERSISTENT_CTAS_PER_SM 3
 #endif
+// tensor-core (query-head group) variant: consumer warps per CTA, ring slots
+// per consumer warp, resident CTAs per SM
+#ifndef PKV_MMA_CONSUMER_WARPS
+#define PKV_MMA_CONSUMER_WARPS 2
+#endif
+#ifndef PKV_MMA_SLOTS_PER_WARP
+#define PKV_MMA_SLOTS_PER_WARP 2
+#endif
+#ifndef PKV_MMA_CTAS_PER_SM
+#define PKV_MMA_CTAS_PER_SM 3
+#endif
 
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
@@ -547,17 +558,27 @@ struct StageMeta {
     int pad;
 };
 
-template <int D, int G, typename T> struct PLayout {
-    using Gm = Geometry<D>;
-    static constexpr int NQ = Gm::NSTAGE / kConsumerWarps;            // query buffers (see the producer)
+// Shape of the persistent kernel: W consumer warps with R ring slots each
+// (NSTAGE = W * R, so every slot belongs to one warp), one producer warp,
+// CTAS resident CTAs per SM.
+template <int D, int G, bool MMA> struct PConf {
+    static constexpr int W = MMA ? PKV_MMA_CONSUMER_WARPS : kConsumerWarps;
+    static constexpr int R = MMA ? PKV_MMA_SLOTS_PER_WARP : Geometry<D>::SLOTS_PER_WARP;
+    static constexpr int NSTAGE = W * R;
+    static constexpr int THREADS = (W + 1) * 32;
+    static constexpr int CTAS = MMA ? PKV_MMA_CTAS_PER_SM : persistent_ctas<G>();
+};
+
+template <int D, int G, typename T, bool MMA> struct PLayout {
+    using C = PConf<D, G, MMA>;
+    static constexpr int NQ = C::R;                                   // query buffers (see the producer)
     static constexpr size_t ring = 0;
-    static constexpr size_t qs = ring + (size_t)Gm::NSTAGE * 2 * Gm::STAGE_ELEMS * sizeof(T);
-    static constexpr size_t merge = qs + (size_t)NQ * kConsumerWarps * G * D * sizeof(T);
-    static constexpr size_t bars = merge + (size_t)2 * kConsumerWarps * G * (D + 2) * sizeof(float);
-    static constexpr size_t meta = bars + (size_t)(2 * Gm::NSTAGE + 2) * sizeof(uint64_t);
-    static constexpr size_t seqs = meta + (size_t)Gm::NSTAGE * sizeof(StageMeta);
-    // + 1024: the kernel moves its base up to the next 1024-byte boundary
-    static size_t bytes(int S) { return seqs + (size_t)(2 * S + 1) * sizeof(int) + 1024; }
+    static constexpr size_t qs = ring + (size_t)C::NSTAGE * 2 * Geometry<D>::STAGE_ELEMS * sizeof(T);
+    static constexpr size_t merge = qs + (size_t)NQ * C::W * G * D * sizeof(T);
+    static constexpr size_t bars = merge + (size_t)2 * C::W * G * (D + 2) * sizeof(float);
+    static constexpr size_t meta = bars + (size_t)(2 * C::NSTAGE + 2) * sizeof(uint64_t);
+    static constexpr size_t seqs = meta + (size_t)C::NSTAGE * sizeof(StageMeta);
+    static size_t bytes(int S) { return seqs + (size_t)(2 * S + 1) * sizeof(int); }
 };
 
 // In place: v[1..n] := inclusive prefix sums of v[1..n]; v[0] := 0.
@@ -596,7 +617,7 @@ struct Item {
 
 // Ticket t -> item: t / tiles indexes the partitions of all sequences in
 // order (pref holds their prefix sums), t % tiles the query-head tile.
-template <int G>
+template <int G, int W>
 __device__ __forceinline__ void decode_item(const AttnArgs &a, const int *pref, const int *ctxs, int S, int tiles,
                                             unsigned int t, int lane, Item &it) {
     const int pidx = (int)(t / (unsigned int)tiles);
@@ -616,7 +637,7 @@ __device__ __forceinline__ void decode_item(const AttnArgs &a, const int *pref, 
     int ntok = ctx - it.tok0 < a.partition ? ctx - it.tok0 : a.partition;
     it.ntok = ntok < 0 ? 0 : ntok;
     it.nst = (it.ntok + kStageRows - 1) / kStageRows;
-    it.npad = ((it.nst > 0 ? it.nst : 1) + kConsumerWarps - 1) / kConsumerWarps * kConsumerWarps;
+    it.npad = ((it.nst > 0 ? it.nst : 1) + W - 1) / W * W;
     it.nblk = (ctx + (1 << a.log2_block) - 1) >> a.log2_block;
     it.win = it.tok0 >> a.log2_block;
     const int j = it.win + lane;
@@ -627,16 +648,16 @@ __device__ __forceinline__ void decode_item(const AttnArgs &a, const int *pref, 
 // tiled TMA copies through tmk / tmv; otherwise the CUDA-core stage fed by
 // 1-D bulk copies (tmk / tmv unused).
 template <int D, int G, typename T, bool MMA>
-__global__ void __launch_bounds__(kThreads, persistent_ctas<G>())
+__global__ void __launch_bounds__(PConf<D, G, MMA>::THREADS, PConf<D, G, MMA>::CTAS)
     paged_attention_persistent_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmk,
                                       const __grid_constant__ CUtensorMap tmv) {
     using Gm = Geometry<D>;
-    using L = PLayout<D, G, T>;
-    constexpr int NSTAGE = Gm::NSTAGE, SE = Gm::STAGE_ELEMS, LPR = Gm::LPR, W = kConsumerWarps;
+    using L = PLayout<D, G, T, MMA>;
+    using Cf = PConf<D, G, MMA>;
+    constexpr int NSTAGE = Cf::NSTAGE, SE = Gm::STAGE_ELEMS, LPR = Gm::LPR, W = Cf::W;
     constexpr int NQ = L::NQ;
-    extern __shared__ __align__(1024) unsigned char smem_raw[];
     // the 128-byte swizzle repeats every 1024 bytes: the ring starts on such a boundary
-    unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    extern __shared__ __align__(1024) unsigned char smem[];
     T *ring = reinterpret_cast<T *>(smem + L::ring);                 // [NSTAGE][2][32][D]
     T *qs = reinterpret_cast<T *>(smem + L::qs);                     // [NQ][W][G][D]
     float *mg = reinterpret_cast<float *>(smem + L::merge);          // [2][W][G][D + 2]: o, m, l
@@ -664,7 +685,8 @@ __global__ void __launch_bounds__(kThreads, persistent_ctas<G>())
     }
     pdl_trigger();
     pdl_wait();
-    if (threadIdx.x == 0) cta_flags = (timed_out(a.st) ? 1 : 0) | (hdr->magic != kWsMagic ? 2 : 0);
+    if (threadIdx.x == 0)
+        cta_flags = (timed_out(a.st) ? 1 : 0) | (hdr->magic != kWsMagic ? 2 : 0) | ((smem_u32(smem) & 1023u) ? 4 : 0);
     for (int i = threadIdx.x; i < S; i += blockDim.x) {
         int c = a.ctx_lens[i];
         if (c < 0 || c > a.max_ctx) {
@@ -677,6 +699,7 @@ __global__ void __launch_bounds__(kThreads, persistent_ctas<G>())
     __syncthreads();
     if (cta_flags) {                                   // uniform over the CTA
         if ((cta_flags & 2) && blockIdx.x == 0 && threadIdx.x == 0) latch(a.st, kFlagBadWorkspace, hdr->magic);
+        if ((cta_flags & 4) && blockIdx.x == 0 && threadIdx.x == 0) latch(a.st, kFlagTimeout, -2);
         return;
     }
     block_prefix_sum(pref, S);
@@ -701,12 +724,12 @@ __global__ void __launch_bounds__(kThreads, persistent_ctas<G>())
         unsigned int nxt_raw = 0;
         if (lane == 0) nxt_raw = gridDim.x + atomicAdd(&hdr->next, 1u);
         Item cur, nx;
-        if (cur_t < N) decode_item<G>(a, pref, ctxs, S, tiles, cur_t, lane, cur);
+        if (cur_t < N) decode_item<G, W>(a, pref, ctxs, S, tiles, cur_t, lane, cur);
         int kk = 0, items = 0;
         bool dead = false;
         while (cur_t < N && !dead) {
             const unsigned int nxt_t = __shfl_sync(kFull, nxt_raw, 0);
-            if (nxt_t < N) decode_item<G>(a, pref, ctxs, S, tiles, nxt_t, lane, nx);
+            if (nxt_t < N) decode_item<G, W>(a, pref, ctxs, S, tiles, nxt_t, lane, nx);
             if (lane == 0) nxt_raw = gridDim.x + atomicAdd(&hdr->next, 1u);
             const int s = cur.s, part = cur.part, nparts = cur.nparts, g = cur.g, h0 = cur.h0;
             const int tok0 = cur.tok0, ntok = cur.ntok, nst = cur.nst, npad = cur.npad, nblk = cur.nblk;
@@ -972,28 +995,65 @@ __global__ void __launch_bounds__(kThreads, persistent_ctas<G>())
 
 // Merge the partitions of each (sequence, head) with more than one:
 // M = max_p m_p, L = sum_p l_p 2^(m_p - M), out = sum_p o_p 2^(m_p - M) / L.
+// One CTA per (head, sequence); kReduceThreads / D groups of D threads split
+// the partitions between them (thread e of a group owns output element e),
+// so that many partial rows are in flight at once.
+constexpr int kReduceThreads = 256;
+constexpr int kReduceChunk = 1024;                  // partition weights staged per pass
+
 template <int D, typename T>
-__global__ void __launch_bounds__(D) partition_reduce_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(kReduceThreads) partition_reduce_kernel(const AttnArgs a) {
+    constexpr int NG = kReduceThreads / D;
+    __shared__ float wsh[kReduceChunk];
+    __shared__ float red[kReduceThreads / 32];
+    __shared__ float opart[NG][D];
     pdl_trigger();
     pdl_wait();
-    const int h = blockIdx.x, s = blockIdx.y, e = threadIdx.x;
+    const int h = blockIdx.x, s = blockIdx.y, tid = threadIdx.x;
     int ctx = a.ctx_lens[s];
     ctx = ctx < 0 ? 0 : (ctx > a.max_ctx ? a.max_ctx : ctx);
     const int np = (ctx + a.partition - 1) / a.partition;
-    if (np <= 1) return;
+    if (np <= 1) return;                            // uniform over the CTA
     const size_t base = ((size_t)s * a.num_heads + h) * a.max_parts;
     const float *m = a.ws_m + base;
     const float *l = a.ws_l + base;
     const float *o = a.ws_o + base * D;
-    float M = -INFINITY;
-    for (int p = 0; p < np; p++) M = fmaxf(M, m[p]);
-    float L = 0.f, O = 0.f;
-    for (int p = 0; p < np; p++) {
-        const float wt = exp2f(m[p] - M);
-        L = fmaf(l[p], wt, L);
-        O = fmaf(o[(size_t)p * D + e], wt, O);
+    // M
+    float mx = -INFINITY;
+    for (int p = tid; p < np; p += kReduceThreads) mx = fmaxf(mx, m[p]);
+    mx = warp_max(mx);
+    if ((tid & 31) == 0) red[tid >> 5] = mx;
+    __syncthreads();
+    float M = red[0];
+#pragma unroll
+    for (int w = 1; w < kReduceThreads / 32; w++) M = fmaxf(M, red[w]);
+    __syncthreads();
+    const int grp = tid / D, e = tid % D;
+    float Lp = 0.f, O = 0.f;
+    for (int p0 = 0; p0 < np; p0 += kReduceChunk) {
+        const int n = np - p0 < kReduceChunk ? np - p0 : kReduceChunk;
+        for (int p = tid; p < n; p += kReduceThreads) {
+            const float wt = exp2f(m[p0 + p] - M);
+            wsh[p] = wt;
+            Lp = fmaf(l[p0 + p], wt, Lp);
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int p = grp; p < n; p += NG) O = fmaf(wsh[p], o[(size_t)(p0 + p) * D + e], O);
+        __syncthreads();
     }
-    static_cast<T *>(a.out)[((size_t)s * a.num_heads + h) * D + e] = F16Traits<T>::from_f32(L > 0.f ? O / L : 0.f);
+    Lp = warp_sum(Lp);
+    if ((tid & 31) == 0) red[tid >> 5] = Lp;
+    opart[grp][e] = O;
+    __syncthreads();
+    if (grp == 0) {
+        float L = 0.f;
+#pragma unroll
+        for (int w = 0; w < kReduceThreads / 32; w++) L += red[w];
+#pragma unroll
+        for (int g = 1; g < NG; g++) O += opart[g][e];
+        static_cast<T *>(a.out)[((size_t)s * a.num_heads + h) * D + e] = F16Traits<T>::from_f32(L > 0.f ? O / L : 0.f);
+    }
 }
 
 constexpr int kDefaultPartition = 512;
@@ -1062,7 +1122,8 @@ bool encode_cache_map(CUtensorMap *map, const void *base, int num_blocks, int Hk
 
 template <int D, int G, typename T, bool MMA>
 cudaError_t launch_persistent(const AttnArgs &a, dim3 grid, cudaStream_t st) {
-    const size_t psmem = PLayout<D, G, T>::bytes(a.num_seqs);
+    using Cf = PConf<D, G, MMA>;
+    const size_t psmem = PLayout<D, G, T, MMA>::bytes(a.num_seqs);
     static size_t configured_p = 0;          // largest size set so far for this instance
     auto kern = paged_attention_persistent_kernel<D, G, T, MMA>;
     if (psmem > configured_p) {
@@ -1081,29 +1142,14 @@ cudaError_t launch_persistent(const AttnArgs &a, dim3 grid, cudaStream_t st) {
     }
     // enough CTAs to fill the GPU, never more than there can be items
     const long long items = (long long)grid.x * grid.y * grid.z;
-    long long ctas = (long long)sm_count() * persistent_ctas<G>();
+    long long ctas = (long long)sm_count() * Cf::CTAS;
     if (ctas > items) ctas = items;
-    return launch(kern, dim3((unsigned)ctas), dim3(kThreads), psmem, st, a, tmk, tmv);
+    return launch(kern, dim3((unsigned)ctas), dim3(Cf::THREADS), psmem, st, a, tmk, tmv);
 }
 
 template <int D, int G, typename T> cudaError_t launch_attention(const AttnArgs &a, dim3 grid, cudaStream_t st) {
-    const size_t psmem = PLayout<D, G, T>::bytes(a.num_seqs);
-    if (a.num_seqs <= kMaxPersistentSeqs && psmem <= kMaxSmemPerCta) {
-        static size_t configured_p = 0;      // largest size set so far for this instance
-        auto kern = paged_attention_persistent_kernel<D, G, T, false>;
-        if (psmem > configured_p) {
-            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
-            if (e != cudaSuccess) return e;
-            configured_p = psmem;
-        }
-        // enough CTAs to fill the GPU, never more than there can be items
-        const long long items = (long long)grid.x * grid.y * grid.z;
-        long long ctas = (long long)sm_count() * persistent_ctas<G>();
-        if (ctas > items) ctas = items;
-        CUtensorMap none;
-        std::memset(&none, 0, sizeof none);
-        return launch(kern, dim3((unsigned)ctas), dim3(kThreads), psmem, st, a, none, none);
-    }
+    if (a.num_seqs <= kMaxPersistentSeqs && PLayout<D, G, T, false>::bytes(a.num_seqs) <= kMaxSmemPerCta)
+        return launch_persistent<D, G, T, false>(a, grid, st);
     static bool configured = false;
     auto kern = paged_attention_kernel<D, G, T>;
     const size_t smem = smem_bytes<D, T>();
@@ -1131,11 +1177,13 @@ bool use_persistent(int num_seqs, int D, int G, int esize) {
     if (num_seqs > kMaxPersistentSeqs) return false;
     size_t need = 0;
     if (D == 64)
-        need = G == 8 ? PLayout<64, 8, __half>::bytes(num_seqs) : G == 4 ? PLayout<64, 4, __half>::bytes(num_seqs)
-                                                                      : PLayout<64, 2, __half>::bytes(num_seqs);
+        need = G == 8   ? PLayout<64, 8, __half, true>::bytes(num_seqs)
+               : G == 4 ? PLayout<64, 4, __half, true>::bytes(num_seqs)
+                        : PLayout<64, 2, __half, false>::bytes(num_seqs);
     else
-        need = G == 8 ? PLayout<128, 8, __half>::bytes(num_seqs) : G == 4 ? PLayout<128, 4, __half>::bytes(num_seqs)
-                                                                       : PLayout<128, 2, __half>::bytes(num_seqs);
+        need = G == 8   ? PLayout<128, 8, __half, true>::bytes(num_seqs)
+               : G == 4 ? PLayout<128, 4, __half, true>::bytes(num_seqs)
+                        : PLayout<128, 2, __half, false>::bytes(num_seqs);
     return need <= kMaxSmemPerCta;
 }
 
@@ -1155,8 +1203,8 @@ template <typename T> cudaError_t dispatch_d(int D, int G, const AttnArgs &a, di
 }
 
 template <typename T> cudaError_t launch_reduce(int D, const AttnArgs &a, dim3 grid, cudaStream_t st) {
-    if (D == 64) return launch(partition_reduce_kernel<64, T>, grid, dim3(64), 0, st, a);
-    return launch(partition_reduce_kernel<128, T>, grid, dim3(128), 0, st, a);
+    if (D == 64) return launch(partition_reduce_kernel<64, T>, grid, dim3(kReduceThreads), 0, st, a);
+    return launch(partition_reduce_kernel<128, T>, grid, dim3(kReduceThreads), 0, st, a);
 }
 
 }  // namespace
