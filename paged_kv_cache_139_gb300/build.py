@@ -33,8 +33,8 @@ def _nvcc() -> str:
     return str(_cuda_home() / "bin" / "nvcc")
 
 
-def _sources():
-    return [CSRC / s for s in CUDA_SOURCES + CXX_SOURCES]
+def _sources(src_dir: pathlib.Path = CSRC):
+    return [src_dir / s for s in CUDA_SOURCES + CXX_SOURCES]
 
 
 def _headers():
@@ -52,11 +52,12 @@ def _compile(src: pathlib.Path, verbose: bool, obj_dir: pathlib.Path = OBJ, defi
     obj = obj_dir / (src.name + ".o")
     if src.suffix == ".cu":
         cmd = [_nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
-               "-I", str(INCLUDE), "-I", str(CSRC), *[f"-D{d}" for d in defines], "-c", str(src), "-o", str(obj)]
+               "-I", str(INCLUDE), "-I", str(src.parent), *[f"-D{d}" for d in defines], "-c", str(src), "-o",
+               str(obj)]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
     else:
-        cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", "-I", str(INCLUDE), "-I", str(CSRC),
+        cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", "-I", str(INCLUDE), "-I", str(src.parent),
                "-I", str(_cuda_home() / "include"), "-c", str(src), "-o", str(obj)]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -66,9 +67,10 @@ def _compile(src: pathlib.Path, verbose: bool, obj_dir: pathlib.Path = OBJ, defi
     return obj
 
 
-def build(force: bool = False, verbose: bool = False, out: pathlib.Path = None, defines=()) -> pathlib.Path:
-    """Build the library (by default in-tree); `out` and `defines` build a
-    variant with tuning knobs set, elsewhere."""
+def build(force: bool = False, verbose: bool = False, out: pathlib.Path = None, defines=(),
+          src_dir: pathlib.Path = CSRC) -> pathlib.Path:
+    """Build the library (by default in-tree); `out`, `defines` and `src_dir`
+    build a variant (tuning knobs set, or another source tree) elsewhere."""
     lib = LIB if out is None else pathlib.Path(out)
     if out is None and not defines and not force and not _stale():
         return LIB
@@ -76,7 +78,7 @@ def build(force: bool = False, verbose: bool = False, out: pathlib.Path = None, 
     obj_dir.mkdir(parents=True, exist_ok=True)
     lib.parent.mkdir(parents=True, exist_ok=True)
     with ThreadPoolExecutor(max_workers=len(_sources())) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose, obj_dir, defines), _sources()))
+        objs = list(ex.map(lambda s: _compile(s, verbose, obj_dir, defines), _sources(pathlib.Path(src_dir))))
     tmp = lib.parent / f"libpkv.{os.getpid()}.so"
     cmd = [_nvcc(), *ARCH, "-shared", "-o", str(tmp), *map(str, objs), "-lcudart_static", "-lrt", "-ldl",
            "-lpthread"]

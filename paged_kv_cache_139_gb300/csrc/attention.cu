@@ -54,10 +54,10 @@ namespace {
 // tensor-core (query-head group) variant: consumer warps per CTA, ring slots
 // per consumer warp, resident CTAs per SM
 #ifndef PKV_MMA_CONSUMER_WARPS
-#define PKV_MMA_CONSUMER_WARPS 2
+#define PKV_MMA_CONSUMER_WARPS 1
 #endif
 #ifndef PKV_MMA_SLOTS_PER_WARP
-#define PKV_MMA_SLOTS_PER_WARP 2
+#define PKV_MMA_SLOTS_PER_WARP 4
 #endif
 #ifndef PKV_MMA_CTAS_PER_SM
 #define PKV_MMA_CTAS_PER_SM 3
@@ -178,6 +178,71 @@ __device__ __forceinline__ void consume_stage(const T *Ks, const T *Vs, int nval
     }
 }
 
+// The persistent kernel's CUDA-core stage: as consume_stage, but QK^T runs as
+// fp32-accumulating FMAs straight on the 16-bit q and k values (no
+// conversions; the score is scaled afterwards) and PV on pairs of fp32 lanes.
+// qw[h][j] holds the two 16-bit query values j of the lane's chunk.
+template <int D, int G, typename T, bool FULL_STAGE>
+__device__ __forceinline__ void consume_stage_v2(const T *Ks, const T *Vs, int nvalid, int r, int c,
+                                                 const uint32_t (&qw)[G][4], float scale_log2, float (&m)[G],
+                                                 float (&lsum)[G], unsigned long long (&acc)[G][4]) {
+    using Gm = Geometry<D>;
+    constexpr int NI = Gm::NI, RPI = Gm::RPI, LPR = Gm::LPR;
+    float part[G][NI];
+#pragma unroll
+    for (int i = 0; i < NI; i++) {
+        const int row = i * RPI + r;
+        const uint4 raw = *reinterpret_cast<const uint4 *>(Ks + row * D + c * 8);
+        const uint32_t kw[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int h = 0; h < G; h++) {
+            float a = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                a = fma_mixed<T>((unsigned short)(qw[h][j] & 0xffffu), (unsigned short)(kw[j] & 0xffffu), a);
+                a = fma_mixed<T>((unsigned short)(qw[h][j] >> 16), (unsigned short)(kw[j] >> 16), a);
+            }
+            part[h][i] = a;
+        }
+    }
+    const int myrow = c * RPI + r;
+    float p[G];
+#pragma unroll
+    for (int h = 0; h < G; h++) {
+        float sc = reduce_scatter<NI>(part[h], c) * scale_log2;
+        if (!FULL_STAGE && myrow >= nvalid) sc = -INFINITY;
+        const float mnew = fmaxf(m[h], warp_max(sc));
+        const float alpha = exp2f(m[h] - mnew);
+        p[h] = exp2f(sc - mnew);
+        lsum[h] = lsum[h] * alpha + p[h];
+        const unsigned long long a2 = pack2(alpha, alpha);
+#pragma unroll
+        for (int j = 0; j < 4; j++) acc[h][j] = mul2(acc[h][j], a2);
+        m[h] = mnew;
+    }
+#pragma unroll
+    for (int i = 0; i < NI; i++) {
+        const int row = i * RPI + r;
+        const uint4 raw = *reinterpret_cast<const uint4 *>(Vs + row * D + c * 8);
+        float vf[8];
+        F16Traits<T>::to_f32(raw, vf);
+        if (!FULL_STAGE && row >= nvalid) {
+#pragma unroll
+            for (int e = 0; e < 8; e++) vf[e] = 0.f;      // rows past the context may hold anything
+        }
+        unsigned long long v2[4];
+#pragma unroll
+        for (int j = 0; j < 4; j++) v2[j] = pack2(vf[2 * j], vf[2 * j + 1]);
+#pragma unroll
+        for (int h = 0; h < G; h++) {
+            const float w = __shfl_sync(kFull, p[h], r * LPR + i);
+            const unsigned long long w2 = pack2(w, w);
+#pragma unroll
+            for (int j = 0; j < 4; j++) acc[h][j] = fma2(w2, v2[j], acc[h][j]);
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Tensor-core stage for query-head groups (GQA): the G heads of one kv head
 // form the rows of a 16 x d query tile, so QK^T and PV become m16n8k16 MMAs
@@ -239,11 +304,12 @@ __device__ __forceinline__ void consume_stage_mma(const T *Ks, T *Vs, int nvalid
         __syncwarp();
     }
     // S = Q K^T: 4 column tiles of 8 tokens
-    float s[4][4];
+    // two accumulator sets (even and odd k-steps) halve the dependent MMA chain
+    float s[4][4], s2[4][4];
 #pragma unroll
     for (int nt = 0; nt < 4; nt++)
 #pragma unroll
-        for (int e = 0; e < 4; e++) s[nt][e] = 0.f;
+        for (int e = 0; e < 4; e++) s[nt][e] = s2[nt][e] = 0.f;
 #pragma unroll
     for (int kp = 0; kp < D / 32; kp++) {
 #pragma unroll
@@ -253,9 +319,13 @@ __device__ __forceinline__ void consume_stage_mma(const T *Ks, T *Vs, int nvalid
             const uint32_t a0[4] = {qa[2 * kp][0], 0u, qa[2 * kp][1], 0u};
             const uint32_t a1[4] = {qa[2 * kp + 1][0], 0u, qa[2 * kp + 1][1], 0u};
             Mma<T>::run(s[nt], a0, b[0], b[1]);
-            Mma<T>::run(s[nt], a1, b[2], b[3]);
+            Mma<T>::run(s2[nt], a1, b[2], b[3]);
         }
     }
+#pragma unroll
+    for (int nt = 0; nt < 4; nt++)
+#pragma unroll
+        for (int e = 0; e < 4; e++) s[nt][e] += s2[nt][e];
     // online softmax over the row's 8 tokens on this lane (a quad holds the row)
     float x[8];
 #pragma unroll
@@ -577,13 +647,14 @@ template <int D, int G, typename T, bool MMA> struct PLayout {
     static constexpr size_t merge = qs + (size_t)NQ * C::W * G * D * sizeof(T);
     static constexpr size_t bars = merge + (size_t)2 * C::W * G * (D + 2) * sizeof(float);
     static constexpr size_t meta = bars + (size_t)(2 * C::NSTAGE + 2) * sizeof(uint64_t);
-    static constexpr size_t seqs = meta + (size_t)C::NSTAGE * sizeof(StageMeta);
+    static constexpr size_t misc = meta + (size_t)C::NSTAGE * sizeof(StageMeta);   // flags + scan scratch
+    static constexpr size_t seqs = misc + 64 * sizeof(int);
     static size_t bytes(int S) { return seqs + (size_t)(2 * S + 1) * sizeof(int); }
 };
 
 // In place: v[1..n] := inclusive prefix sums of v[1..n]; v[0] := 0.
-__device__ __forceinline__ void block_prefix_sum(int *v, int n) {
-    __shared__ int warp_tot[32];
+// warp_tot: shared scratch of one int per warp.
+__device__ __forceinline__ void block_prefix_sum(int *v, int n, int *warp_tot) {
     const int nt = blockDim.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int chunk = (n + nt - 1) / nt;
     const int b0 = tid * chunk < n ? tid * chunk : n;
@@ -657,7 +728,8 @@ __global__ void __launch_bounds__(PConf<D, G, MMA>::THREADS, PConf<D, G, MMA>::C
     constexpr int NSTAGE = Cf::NSTAGE, SE = Gm::STAGE_ELEMS, LPR = Gm::LPR, W = Cf::W;
     constexpr int NQ = L::NQ;
     // the 128-byte swizzle repeats every 1024 bytes: the ring starts on such a boundary
-    extern __shared__ __align__(1024) unsigned char smem[];
+    extern __shared__ __align__(1024) unsigned char smem_p[];
+    unsigned char *smem = smem_p;
     T *ring = reinterpret_cast<T *>(smem + L::ring);                 // [NSTAGE][2][32][D]
     T *qs = reinterpret_cast<T *>(smem + L::qs);                     // [NQ][W][G][D]
     float *mg = reinterpret_cast<float *>(smem + L::merge);          // [2][W][G][D + 2]: o, m, l
@@ -668,7 +740,8 @@ __global__ void __launch_bounds__(PConf<D, G, MMA>::THREADS, PConf<D, G, MMA>::C
     const int S = a.num_seqs;
     int *pref = reinterpret_cast<int *>(smem + L::seqs);             // [S + 1] partitions before s
     int *ctxs = pref + S + 1;                                        // [S]
-    __shared__ int cta_flags;
+    int &cta_flags = *reinterpret_cast<int *>(smem + L::misc);
+    int *scan_tmp = reinterpret_cast<int *>(smem + L::misc) + 32;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tiles = a.num_kv_heads * a.head_tiles;
@@ -702,7 +775,7 @@ __global__ void __launch_bounds__(PConf<D, G, MMA>::THREADS, PConf<D, G, MMA>::C
         if ((cta_flags & 4) && blockIdx.x == 0 && threadIdx.x == 0) latch(a.st, kFlagTimeout, -2);
         return;
     }
-    block_prefix_sum(pref, S);
+    block_prefix_sum(pref, S, scan_tmp);
     const unsigned int N = (unsigned int)pref[S] * (unsigned int)tiles;
     const int B = 1 << a.log2_block;
 
@@ -854,7 +927,9 @@ __global__ void __launch_bounds__(PConf<D, G, MMA>::THREADS, PConf<D, G, MMA>::C
 
     // ---------------- consumers ----------------
     const int r = lane / LPR, c = lane % LPR;
-    float qf[G][8], m[G], lsum[G], acc[G][8];          // CUDA-core stage state
+    uint32_t qw[G][4];                                 // CUDA-core stage state
+    float m[G], lsum[G];
+    unsigned long long acc[G][4];
     uint32_t qa[D / 16][2];                            // tensor-core stage state
     MmaState<D> ms;
     auto reset = [&]() {
@@ -866,7 +941,7 @@ __global__ void __launch_bounds__(PConf<D, G, MMA>::THREADS, PConf<D, G, MMA>::C
                 m[h] = -INFINITY;
                 lsum[h] = 0.f;
 #pragma unroll
-                for (int e = 0; e < 8; e++) acc[h][e] = 0.f;
+                for (int j = 0; j < 4; j++) acc[h][j] = 0ull;
             }
         }
     };
@@ -900,15 +975,16 @@ __global__ void __launch_bounds__(PConf<D, G, MMA>::THREADS, PConf<D, G, MMA>::C
 #pragma unroll
                 for (int h = 0; h < G; h++) {
                     const uint4 raw = *reinterpret_cast<const uint4 *>(qp + h * D + c * 8);
-                    F16Traits<T>::to_f32(raw, qf[h]);
-#pragma unroll
-                    for (int e = 0; e < 8; e++) qf[h][e] *= a.scale_log2;
+                    qw[h][0] = raw.x;
+                    qw[h][1] = raw.y;
+                    qw[h][2] = raw.z;
+                    qw[h][3] = raw.w;
                 }
             }
             if (md.nvalid == kStageRows)
-                consume_stage<D, G, T, true>(Ks, Ks + SE, md.nvalid, r, c, qf, m, lsum, acc);
+                consume_stage_v2<D, G, T, true>(Ks, Ks + SE, md.nvalid, r, c, qw, a.scale_log2, m, lsum, acc);
             else if (md.nvalid > 0)
-                consume_stage<D, G, T, false>(Ks, Ks + SE, md.nvalid, r, c, qf, m, lsum, acc);
+                consume_stage_v2<D, G, T, false>(Ks, Ks + SE, md.nvalid, r, c, qw, a.scale_log2, m, lsum, acc);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
@@ -934,20 +1010,26 @@ __global__ void __launch_bounds__(PConf<D, G, MMA>::THREADS, PConf<D, G, MMA>::C
                 }
             }
         } else {
+            float accf[G][8];
 #pragma unroll
             for (int h = 0; h < G; h++) {
                 lsum[h] = warp_sum(lsum[h]);
 #pragma unroll
+                for (int j = 0; j < 4; j++) {
+                    accf[h][2 * j] = lo2(acc[h][j]);
+                    accf[h][2 * j + 1] = hi2(acc[h][j]);
+                }
+#pragma unroll
                 for (int e = 0; e < 8; e++) {
 #pragma unroll
-                    for (int o = LPR; o < 32; o <<= 1) acc[h][e] += __shfl_xor_sync(kFull, acc[h][e], o);
+                    for (int o = LPR; o < 32; o <<= 1) accf[h][e] += __shfl_xor_sync(kFull, accf[h][e], o);
                 }
             }
             if (r == 0) {
 #pragma unroll
                 for (int h = 0; h < G; h++)
 #pragma unroll
-                    for (int e = 0; e < 8; e++) mw[h * (D + 2) + c * 8 + e] = acc[h][e];
+                    for (int e = 0; e < 8; e++) mw[h * (D + 2) + c * 8 + e] = accf[h][e];
             }
             if (lane == 0) {
 #pragma unroll

@@ -155,6 +155,39 @@ __device__ __forceinline__ void tma_load_4d(void *smem_dst, const void *tmap, in
         : "memory");
 }
 
+// ---- fp32 arithmetic on 16-bit inputs and on pairs ---------------------------
+
+// a * b + c with 16-bit a, b (bit patterns) and fp32 c, d: the inputs widen
+// exactly, so the result equals fmaf((float)a, (float)b, c).
+template <typename T> __device__ __forceinline__ float fma_mixed(unsigned short a, unsigned short b, float c);
+template <> __device__ __forceinline__ float fma_mixed<__half>(unsigned short a, unsigned short b, float c) {
+    float d;
+    asm("fma.rn.f32.f16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
+    return d;
+}
+template <> __device__ __forceinline__ float fma_mixed<__nv_bfloat16>(unsigned short a, unsigned short b, float c) {
+    float d;
+    asm("fma.rn.f32.bf16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
+    return d;
+}
+
+// Two fp32 lanes at once.
+__device__ __forceinline__ unsigned long long pack2(float x, float y) {
+    return (unsigned long long)__float_as_uint(x) | ((unsigned long long)__float_as_uint(y) << 32);
+}
+__device__ __forceinline__ float lo2(unsigned long long v) { return __uint_as_float((unsigned)v); }
+__device__ __forceinline__ float hi2(unsigned long long v) { return __uint_as_float((unsigned)(v >> 32)); }
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b, unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // ---- warp-level tensor-core fragments ---------------------------------------
 
 // Four 8x8 16-bit matrices; lane L gives the row address of matrix L / 8.
