@@ -63,6 +63,11 @@ namespace {
 #define PKV_MMA_CTAS_PER_SM 3
 #endif
 
+// consumer warps per CTA of the CUDA-core variants
+#ifndef PKV_SIMT_CONSUMER_WARPS
+#define PKV_SIMT_CONSUMER_WARPS 4
+#endif
+
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStageRows = 32;              // tokens per ring stage
@@ -393,7 +398,32 @@ struct AttnArgs {
     int partition;               // P
     int max_parts;               // MP
     float scale_log2;            // scale * log2(e)
+    unsigned int *cnt;           // [S][H] partitions finished (fused merge); zero between calls
+    int fused_merge;             // 1: the last partition of a (sequence, head tile) merges them all
 };
+
+constexpr int kFusedMaxParts = 16;          // longer splits go to partition_reduce_kernel
+
+// The partitions of query heads h0 .. h0 + G - 1 of sequence s, merged by one
+// warp (log-sum-exp, as partition_reduce_kernel) straight from the workspace.
+// The partials were written by other CTAs: read them past L1.
+template <int D, int G, typename T>
+__device__ __forceinline__ void merge_partitions_warp(const AttnArgs &a, int s, int h0, int np, int lane) {
+#pragma unroll 1
+    for (int h = 0; h < G; h++) {
+        const size_t base = ((size_t)s * a.num_heads + h0 + h) * a.max_parts;
+        const float mp = lane < np ? __ldcg(a.ws_m + base + lane) : -INFINITY;
+        const float M = warp_max(mp);
+        const float wp = lane < np ? exp2f(mp - M) : 0.f;
+        const float L = warp_sum(lane < np ? __ldcg(a.ws_l + base + lane) * wp : 0.f);
+        for (int e = lane; e < D; e += 32) {
+            float O = 0.f;
+            for (int p = 0; p < np; p++) O = fmaf(__shfl_sync(kFull, wp, p), __ldcg(a.ws_o + (base + p) * D + e), O);
+            static_cast<T *>(a.out)[((size_t)s * a.num_heads + h0 + h) * D + e] =
+                F16Traits<T>::from_f32(L > 0.f ? O / L : 0.f);
+        }
+    }
+}
 
 template <int D, int G, typename T>
 __global__ void __launch_bounds__(kThreads, min_ctas<G>()) paged_attention_kernel(const AttnArgs a) {
@@ -632,8 +662,8 @@ struct StageMeta {
 // (NSTAGE = W * R, so every slot belongs to one warp), one producer warp,
 // CTAS resident CTAs per SM.
 template <int D, int G, bool MMA> struct PConf {
-    static constexpr int W = MMA ? PKV_MMA_CONSUMER_WARPS : kConsumerWarps;
-    static constexpr int R = MMA ? PKV_MMA_SLOTS_PER_WARP : Geometry<D>::SLOTS_PER_WARP;
+    static constexpr int W = MMA ? PKV_MMA_CONSUMER_WARPS : PKV_SIMT_CONSUMER_WARPS;
+    static constexpr int R = MMA ? PKV_MMA_SLOTS_PER_WARP : Geometry<D>::SLOTS_PER_WARP * kConsumerWarps / W;
     static constexpr int NSTAGE = W * R;
     static constexpr int THREADS = (W + 1) * 32;
     static constexpr int CTAS = MMA ? PKV_MMA_CTAS_PER_SM : persistent_ctas<G>();
@@ -790,20 +820,19 @@ __global__ void __launch_bounds__(PConf<D, G, MMA>::THREADS, PConf<D, G, MMA>::C
         const uint32_t q_bytes = (uint32_t)(G * D * sizeof(T));
         const uint64_t policy = policy_evict_first();
         // Tickets: the first item of CTA c is item c; later ones come from the
-        // counter, offset by the grid size.  The next item is decoded (and its
-        // first 32 block-table entries loaded) one item ahead, so the producer
-        // does not wait on the table at item boundaries.
+        // counter, offset by the grid size.  The next ticket is claimed two
+        // stages before the current item's last stage, and decoded (its first
+        // 32 block-table entries loaded) one stage later: late enough that a
+        // CTA never holds a whole unstarted item when the pool runs dry, early
+        // enough to hide the atomic and the block-table load.
         unsigned int cur_t = blockIdx.x;
-        unsigned int nxt_raw = 0;
-        if (lane == 0) nxt_raw = gridDim.x + atomicAdd(&hdr->next, 1u);
         Item cur, nx;
         if (cur_t < N) decode_item<G, W>(a, pref, ctxs, S, tiles, cur_t, lane, cur);
         int kk = 0, items = 0;
         bool dead = false;
         while (cur_t < N && !dead) {
-            const unsigned int nxt_t = __shfl_sync(kFull, nxt_raw, 0);
-            if (nxt_t < N) decode_item<G, W>(a, pref, ctxs, S, tiles, nxt_t, lane, nx);
-            if (lane == 0) nxt_raw = gridDim.x + atomicAdd(&hdr->next, 1u);
+            unsigned int nxt_raw = 0, nxt_t = 0xffffffffu;
+            bool claimed = false, decoded = false;
             const int s = cur.s, part = cur.part, nparts = cur.nparts, g = cur.g, h0 = cur.h0;
             const int tok0 = cur.tok0, ntok = cur.ntok, nst = cur.nst, npad = cur.npad, nblk = cur.nblk;
             const int32_t *trow = a.tables + (size_t)s * a.max_blocks;
@@ -813,68 +842,63 @@ __global__ void __launch_bounds__(PConf<D, G, MMA>::THREADS, PConf<D, G, MMA>::C
             // have been consumed.
             const int qb = items % NQ;
             int win = cur.win, ent = cur.ent;
+            const int i_claim = npad > 2 ? npad - 2 : 0, i_decode = npad > 1 ? npad - 1 : 0;
             for (int i = 0; i < npad; i++, kk++) {
-                int e[8];
-                int off0 = 0;
+                if (i == i_claim) {
+                    if (lane == 0) nxt_raw = gridDim.x + atomicAdd(&hdr->next, 1u);
+                    claimed = true;
+                }
+                if (i == i_decode) {
+                    nxt_t = __shfl_sync(kFull, nxt_raw, 0);
+                    if (nxt_t < N) decode_item<G, W>(a, pref, ctxs, S, tiles, nxt_t, lane, nx);
+                    decoded = true;
+                }
+                const int slot = kk % NSTAGE;
+                const bool withq = i < W && i < nst;               // warp i's first stage of the item
+                // the stage's tokens, blocks and copies (the same on every lane)
+                int nv = 0, nb = 0, off0 = 0, pj = -1;
                 if (i < nst) {                                     // uniform over the warp
                     const int t_first = tok0 + i * kStageRows;
                     const int lb0 = t_first >> a.log2_block;
                     off0 = t_first & (B - 1);
+                    nv = ntok - i * kStageRows < kStageRows ? ntok - i * kStageRows : kStageRows;
+                    nb = (nv + rows_per_copy - 1) / rows_per_copy;
                     if (lb0 < win || lb0 + cps > win + 32) {
                         win = lb0;
                         const int j = win + lane;
                         ent = j < nblk ? __ldg(trow + j) : -1;
                     }
-#pragma unroll
-                    for (int j = 0; j < 8; j++) e[j] = __shfl_sync(kFull, ent, (lb0 + j - win) & 31);
+                    // this lane's block: lane >> 1 (bulk copies) or lane / (2 * halves) (tiled)
+                    const int jl = MMA ? lane / (2 * (D / 64)) : lane >> 1;
+                    pj = __shfl_sync(kFull, ent, (lb0 + jl - win) & 31);
+                    const bool bad = jl < nb && (pj < 0 || pj >= a.num_blocks);
+                    const unsigned badm = __ballot_sync(kFull, bad);
+                    if (badm) {                                    // stop the stage at the first bad block
+                        const int jb = MMA ? (__ffs(badm) - 1) / (2 * (D / 64)) : (__ffs(badm) - 1) >> 1;
+                        if (lane == __ffs(badm) - 1) latch(a.st, kFlagBadBlock, pj);
+                        nb = jb;
+                        nv = jb * rows_per_copy;
+                    }
                 }
-                const int slot = kk % NSTAGE;
-                const bool withq = i < W && i < nst;               // warp i's first stage of the item
-                int ncopies = 0;
+                if (kk >= NSTAGE &&
+                    !__all_sync(kFull, mbar_wait(&empty[slot], ((kk / NSTAGE) - 1) & 1, kWaitLimitCycles))) {
+                    if (lane == 0) latch(a.st, kFlagTimeout, kk);
+                    dead = true;
+                    break;
+                }
                 if (lane == 0) {
-                    if (kk >= NSTAGE && !mbar_wait(&empty[slot], ((kk / NSTAGE) - 1) & 1, kWaitLimitCycles)) {
-                        latch(a.st, kFlagTimeout, kk);
-                        dead = true;
-                    }
-                    if (!dead) {
-                        int nv = 0;
-                        if (i < nst) {
-                            nv = ntok - i * kStageRows < kStageRows ? ntok - i * kStageRows : kStageRows;
-                            for (int j = 0; j < cps && j < 8; j++) {
-                                if (j * rows_per_copy >= nv) break;
-                                const int p = e[j];
-                                if (p < 0 || p >= a.num_blocks) {
-                                    latch(a.st, kFlagBadBlock, p);
-                                    nv = j * rows_per_copy;
-                                    break;
-                                }
-                                ncopies = j + 1;
-                            }
-                        }
-                        StageMeta &m = meta[slot];
-                        m.s = s;
-                        m.h0 = h0;
-                        m.part = part;
-                        m.nparts = nparts;
-                        m.nvalid = nv;
-                        m.qbuf = qb;
-                        m.flags = (i < W ? kMetaFirst : 0) | (i >= npad - W ? kMetaLast : 0);
-                        mbar_arrive_expect_tx(&full[slot], 2u * copy_bytes * (uint32_t)ncopies + (withq ? q_bytes : 0u));
-                    }
+                    int4 *mv = reinterpret_cast<int4 *>(&meta[slot]);
+                    mv[0] = make_int4(s, h0, part, nparts);
+                    mv[1] = make_int4(nv, (i < W ? kMetaFirst : 0) | (i >= npad - W ? kMetaLast : 0), qb, 0);
+                    mbar_arrive_expect_tx(&full[slot], 2u * copy_bytes * (uint32_t)nb + (withq ? q_bytes : 0u));
                 }
-                dead = __shfl_sync(kFull, dead ? 1 : 0, 0) != 0;
-                if (dead) break;
-                ncopies = __shfl_sync(kFull, ncopies, 0);
+                __syncwarp();
                 if (MMA) {
                     // one tiled copy per lane: lane (2j + h) * 2 + t moves half h (64 elements of d)
                     // of block j's K (t = 0) or V (t = 1) tile; lane 0 also moves the query heads
                     constexpr int HALVES = D / 64;
-                    if (lane < ncopies * HALVES * 2) {
+                    if (lane < nb * HALVES * 2) {
                         const int t = lane & 1, h = (lane >> 1) % HALVES, j = (lane >> 1) / HALVES;
-                        int pj = e[0];
-#pragma unroll
-                        for (int x = 1; x < 8; x++)
-                            if (x == j) pj = e[x];
                         T *dst = ring + (size_t)(slot * 2 + t) * SE + h * (kStageRows * 64) + j * rows_per_copy * 64;
                         tma_load_4d(dst, t ? (const void *)&tmv : (const void *)&tmk, h * 64, off0, g, pj, &full[slot],
                                     policy);
@@ -882,21 +906,25 @@ __global__ void __launch_bounds__(PConf<D, G, MMA>::THREADS, PConf<D, G, MMA>::C
                     if (withq && lane == 0)
                         bulk_g2s(qs + (size_t)(qb * W + i) * G * D, qg + ((size_t)s * a.num_heads + h0) * D, q_bytes,
                                  &full[slot]);
-                } else if (lane < 2 * ncopies) {
+                } else {
                     // one bulk copy per lane: lane 2j moves block j's K tile, lane 2j+1 its V tile,
-                    // lane 2 * ncopies the item's query heads
-                    const int j = lane >> 1;
-                    int pj = e[0];
-#pragma unroll
-                    for (int x = 1; x < 8; x++)
-                        if (x == j) pj = e[x];
-                    const size_t goff = (((size_t)pj * a.num_kv_heads + g) * B + off0) * D;
-                    T *dst = ring + (size_t)(slot * 2 + (lane & 1)) * SE + (size_t)j * rows_per_copy * D;
-                    bulk_g2s_hint(dst, ((lane & 1) ? vc : kc) + goff, copy_bytes, &full[slot], policy);
-                } else if (!MMA && withq && lane == 2 * ncopies) {
-                    bulk_g2s(qs + (size_t)(qb * W + i) * G * D, qg + ((size_t)s * a.num_heads + h0) * D, q_bytes,
-                             &full[slot]);
+                    // lane 2 * nb the item's query heads
+                    if (lane < 2 * nb) {
+                        const int j = lane >> 1;
+                        const size_t goff = (((size_t)pj * a.num_kv_heads + g) * B + off0) * D;
+                        T *dst = ring + (size_t)(slot * 2 + (lane & 1)) * SE + (size_t)j * rows_per_copy * D;
+                        bulk_g2s_hint(dst, ((lane & 1) ? vc : kc) + goff, copy_bytes, &full[slot], policy);
+                    } else if (withq && lane == 2 * nb) {
+                        bulk_g2s(qs + (size_t)(qb * W + i) * G * D, qg + ((size_t)s * a.num_heads + h0) * D, q_bytes,
+                                 &full[slot]);
+                    }
                 }
+            }
+            if (dead) break;
+            if (!claimed && lane == 0) nxt_raw = gridDim.x + atomicAdd(&hdr->next, 1u);
+            if (!decoded) {
+                nxt_t = __shfl_sync(kFull, nxt_raw, 0);
+                if (nxt_t < N) decode_item<G, W>(a, pref, ctxs, S, tiles, nxt_t, lane, nx);
             }
             items++;
             cur_t = nxt_t;
@@ -1045,7 +1073,11 @@ __global__ void __launch_bounds__(PConf<D, G, MMA>::THREADS, PConf<D, G, MMA>::C
             break;
         }
         const float *mb = mg + (size_t)b * W * G * (D + 2);
-        for (int idx = warp * 32 + lane; idx < G * D; idx += W * 32) {
+        // one warp combines the item (round robin); the others go on.  Buffer b
+        // is written again two items later, after the next item's barrier,
+        // which this warp reaches only when the combine is done.
+        if (warp == jitem % W) {
+        for (int idx = lane; idx < G * D; idx += 32) {
             const int h = idx / D, e = idx % D;
             float M = -INFINITY;
 #pragma unroll
@@ -1069,6 +1101,21 @@ __global__ void __launch_bounds__(PConf<D, G, MMA>::THREADS, PConf<D, G, MMA>::C
                     a.ws_l[sp] = Lsum;
                 }
             }
+        }
+        if (a.fused_merge && md.nparts > 1) {
+            // count this partition in; the one that completes the set merges it
+            __threadfence();
+            __syncwarp();
+            unsigned int done = 0;
+            unsigned int *cnt = a.cnt + (size_t)md.s * a.num_heads + md.h0;
+            if (lane == 0) done = atomicAdd(cnt, 1u);
+            done = __shfl_sync(kFull, done, 0);
+            if (done == (unsigned int)md.nparts - 1) {
+                __threadfence();
+                merge_partitions_warp<D, G, T>(a, md.s, md.h0, md.nparts, lane);
+                if (lane == 0) *cnt = 0u;
+            }
+        }
         }
         jitem++;
         reset();
@@ -1147,7 +1194,7 @@ int parts_for(int max_ctx, int P) { return max_ctx > 0 ? (max_ctx + P - 1) / P :
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct WsLayout {
-    size_t m_off, l_off, o_off, bytes;
+    size_t m_off, l_off, o_off, cnt_off, bytes;
 };
 
 // Workspace: the ticket header, then (when contexts may span partitions)
@@ -1160,16 +1207,22 @@ WsLayout ws_layout(int S, int H, int D, int MP) {
     w.m_off = kWsHeaderBytes;
     w.l_off = w.m_off + align256(n * sizeof(float));
     w.o_off = w.l_off + align256(n * sizeof(float));
-    w.bytes = w.o_off + align256(n * D * sizeof(float));
+    w.cnt_off = w.o_off + align256(n * D * sizeof(float));
+    w.bytes = w.cnt_off + align256((size_t)S * H * sizeof(unsigned int));
     return w;
 }
 
-__global__ void workspace_init_kernel(WsHeader *h) {
+// Zero the whole workspace, then mark the header initialised.
+__global__ void workspace_init_kernel(uint4 *ws, size_t n16) {
     pdl_trigger();
     pdl_wait();
-    h->next = 0;
-    h->done = 0;
-    h->pad = 0;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x)
+        ws[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+__global__ void workspace_magic_kernel(WsHeader *h) {
+    pdl_trigger();
+    pdl_wait();
     h->magic = kWsMagic;
 }
 
@@ -1309,7 +1362,15 @@ pkv_status paged_attention_workspace_init(void *workspace, size_t workspace_byte
     if (!workspace || workspace_bytes < kWsHeaderBytes || !aligned16(workspace))
         return fail(PKV_EINVAL, "paged_attention_workspace_init: need a 16-byte aligned workspace of at least %zu bytes",
                     kWsHeaderBytes);
-    cudaError_t e = launch(workspace_init_kernel, dim3(1), dim3(1), 0, stream, static_cast<WsHeader *>(workspace));
+    const size_t n16 = workspace_bytes / 16;
+    long long blocks = (long long)((n16 + 255) / 256);
+    const long long cap = (long long)sm_count() * 4;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    cudaError_t e = launch(workspace_init_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
+                           static_cast<uint4 *>(workspace), n16);
+    if (e == cudaSuccess)
+        e = launch(workspace_magic_kernel, dim3(1), dim3(1), 0, stream, static_cast<WsHeader *>(workspace));
     if (e != cudaSuccess) return fail(PKV_ECUDA, "paged_attention_workspace_init: launch: %s", cudaGetErrorString(e));
     return PKV_OK;
 }
@@ -1367,7 +1428,8 @@ pkv_status paged_attention_decode(void *out, const void *query, const void *key_
 
     const int group = num_heads / num_kv_heads;
     int G = head_tile(group, true);
-    if (!use_persistent(num_seqs, head_dim, G, 2)) G = head_tile(group, false);
+    const bool persistent = use_persistent(num_seqs, head_dim, G, 2);
+    if (!persistent) G = head_tile(group, false);
     AttnArgs a;
     a.out = out;
     unsigned char *ws = static_cast<unsigned char *>(workspace);
@@ -1375,6 +1437,7 @@ pkv_status paged_attention_decode(void *out, const void *query, const void *key_
     a.ws_m = MP > 1 ? reinterpret_cast<float *>(ws + wl.m_off) : nullptr;
     a.ws_l = MP > 1 ? reinterpret_cast<float *>(ws + wl.l_off) : nullptr;
     a.ws_o = MP > 1 ? reinterpret_cast<float *>(ws + wl.o_off) : nullptr;
+    a.cnt = MP > 1 ? reinterpret_cast<unsigned int *>(ws + wl.cnt_off) : nullptr;
     a.num_seqs = num_seqs;
     a.q = query;
     a.k_cache = key_cache;
@@ -1392,12 +1455,13 @@ pkv_status paged_attention_decode(void *out, const void *query, const void *key_
     a.partition = P;
     a.max_parts = MP;
     a.scale_log2 = scale * kLog2e;
+    a.fused_merge = persistent && MP > 1 && MP <= kFusedMaxParts;
 
     const dim3 grid((unsigned)(num_kv_heads * a.head_tiles), (unsigned)num_seqs, (unsigned)MP);
     cudaError_t e = dtype == PKV_F16 ? dispatch_d<__half>(head_dim, G, a, grid, stream)
                                      : dispatch_d<__nv_bfloat16>(head_dim, G, a, grid, stream);
     if (e != cudaSuccess) return fail(PKV_ECUDA, "paged_attention_decode: launch: %s", cudaGetErrorString(e));
-    if (MP > 1) {
+    if (MP > 1 && !a.fused_merge) {
         const dim3 rgrid((unsigned)num_heads, (unsigned)num_seqs);
         e = dtype == PKV_F16 ? launch_reduce<__half>(head_dim, a, rgrid, stream)
                              : launch_reduce<__nv_bfloat16>(head_dim, a, rgrid, stream);

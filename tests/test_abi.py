@@ -76,7 +76,8 @@ def test_workspace_size_formula():
     S, H, d, ctx, P = 8, 32, 128, 32768, 512
     n = S * H * (ctx // P)
     r = lambda x: (x + 255) // 256 * 256
-    assert pkv.paged_attention_workspace_size(S, H, 8, d, ctx, P) == 256 + r(4 * n) * 2 + r(4 * n * d)
+    # + one partition counter per (sequence, head)
+    assert pkv.paged_attention_workspace_size(S, H, 8, d, ctx, P) == 256 + r(4 * n) * 2 + r(4 * n * d) + r(4 * S * H)
 
 
 def test_workspace_init_rejects_bad_arguments():

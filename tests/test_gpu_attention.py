@@ -198,13 +198,16 @@ def test_uninitialised_workspace_is_reported(cuda_device):
     assert bool((out == 3.0).all())                                          # nothing was written
 
 
-def test_repeated_calls_reuse_the_workspace(cuda_device):
-    """The ticket counters reset themselves: many calls on one workspace give
-    identical results."""
+@pytest.mark.parametrize("P", [128, 32])
+def test_repeated_calls_reuse_the_workspace(cuda_device, P):
+    """The ticket and partition counters reset themselves: many calls on one
+    workspace give identical results (fused merge at P=128, merge kernel at
+    P=32)."""
     w = _custom(H=8, Hkv=2, ctx=(5, 900, 1500, 31), S=4)
-    c = Case(w, cuda_device, partition_size=128)
+    c = Case(w, cuda_device, partition_size=P)
     outs = [c.rerun_attention().clone() for _ in range(5)]
     assert all(torch.equal(outs[0], o) for o in outs[1:]) and torch.equal(outs[0], c.out)
+    _check(c, what=f"repeat P={P}")
 
 
 def test_bounded_wait_times_out_and_context_survives(cuda_device):
@@ -237,7 +240,13 @@ def test_launch_count_and_native_library(cuda_device):
     before = pkv.launch_count()
     c.eng.decode(c.q_dev, c.k_dev, c.v_dev, c.dev, partition_size=256)
     pkv.check()
-    # cache write + attention + partition merge (the workspace exists already)
+    # cache write + attention; three partitions per sequence merge inside the
+    # attention kernel (the workspace exists already)
+    assert pkv.launch_count() - before == 2
+    # a split into more than 16 partitions adds the merge kernel
+    before = pkv.launch_count()
+    c.eng.decode(c.q_dev, c.k_dev, c.v_dev, c.dev, partition_size=32)
+    pkv.check()
     assert pkv.launch_count() - before == 3
     import os
     maps = open("/proc/self/maps").read()
@@ -254,5 +263,5 @@ def test_prepared_step_matches_decode(cuda_device):
     before = pkv.launch_count()
     prep()
     pkv.check()
-    assert pkv.launch_count() - before == 3
+    assert pkv.launch_count() - before == 2
     assert torch.equal(out, c.out)
