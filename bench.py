@@ -208,6 +208,42 @@ def run_reference(args, rank: int, world: int):
     print(json.dumps(line))
 
 
+def sampling_setup(eng, w: workloads.Workload, dev):
+    """Parallel sampling: each prompt's sequence is forked into its samples
+    (shared blocks), every sample appends its suffix -- the first append into
+    the shared, partly filled last block copies it (copy_blocks) -- and the
+    suffix keys and values are written.  Returns the sample ids and the
+    measured copy-on-write step."""
+    import paged_kv_cache_139_gb300 as pkv
+    n = w.samples_per_prompt
+    ids = []
+    for plen in w.prompt_lens:
+        root = eng.new_sequence(int(plen))
+        ids += [root] + [eng.fork(root) for _ in range(n - 1)]
+    order = []
+    for i, sid in enumerate(ids):
+        order += [sid] * int(w.suffix_lens[i])
+    plan = eng.plan_step(order)
+    dev_plan = eng.upload(plan)
+    sfx = workloads.suffix_tensors(w, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush.zero_()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    eng.copy_on_write(dev_plan.pairs)
+    b.record()
+    eng.write(sfx["key"], sfx["value"], dev_plan.slots)
+    torch.cuda.synchronize(dev)
+    pkv.check()
+    npairs = int(plan.pairs.shape[0])
+    block_bytes = eng.num_kv_heads * eng.block_size * eng.head_dim * eng.key_cache.element_size()
+    ms = a.elapsed_time(b)
+    moved = 2 * 2 * npairs * block_bytes            # K and V, read + write
+    return ids, {"pairs": npairs, "block_bytes": block_bytes, "ms": ms,
+                 "gbs": moved / (ms * 1e-3) / 1e9 if ms > 0 else None, "bytes_moved": moved,
+                 "note": "both copy_blocks launches (K and V) of the suffix step, L2 flushed before"}
+
+
 def aggregate(t_step_ms: float, nbytes: float, dist=None, device="cpu"):
     """Whole-job figures over the ranks: the slowest rank's step time and the
     sum of every rank's bytes (host control traffic only; no data moves)."""
@@ -232,13 +268,15 @@ def run_ours(args, rank: int, world: int):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     w = make_workload(args, rank)
-    if w.prompt_lens is not None:
-        raise SystemExit("bench: the sampling workload is measured by its tests and the copy benchmark")
     t_gpu = workloads.tensors(w, device=dev)
     order = workloads.free_order(w.num_blocks, w.seed)
     eng = PagedKVCache(w.num_blocks, w.num_kv_heads, w.head_dim, w.block_size, w.torch_dtype, dev,
                        w.max_blocks_per_seq, order, key_cache=t_gpu["key_cache"], value_cache=t_gpu["value_cache"])
-    ids = [eng.new_sequence(int(c) - 1) for c in w.context_lens]
+    cow = None
+    if w.prompt_lens is not None:
+        ids, cow = sampling_setup(eng, w, dev)
+    else:
+        ids = [eng.new_sequence(int(c) - 1) for c in w.context_lens]
     plan = eng.plan_step(ids)
     step = eng.upload(plan)
     q, key, value = t_gpu["query"], t_gpu["key"], t_gpu["value"]
@@ -380,7 +418,14 @@ def run_ours(args, rank: int, world: int):
         "wall_s_timed_region": wall,
         "e2e": e2e,
     }
-    if not args.no_cpu_baseline:
+    if cow is not None:
+        B = w.block_size
+        distinct = len({int(b) for row, n in zip(plan.tables, plan.context_lens) for b in row[:-(-int(n) // B)]})
+        unique = distinct * B * w.kv_bytes_per_token
+        line["sharing"] = {"copy_blocks": cow, "unique_kv_bytes_per_step": unique,
+                           "unique_gbs": unique / (t_step_max * 1e-3) / 1e9,
+                           "note": "unique bytes count every distinct physical block in full"}
+    if not args.no_cpu_baseline and cow is None:
         t_cpu = workloads.tensors(w, "cpu")
         line["cpu_baseline"] = cpu_baseline(w, t_cpu, plan.tables, plan.context_lens, plan.slots)
     print(json.dumps(line), flush=True)

@@ -402,13 +402,22 @@ struct AttnArgs {
     int fused_merge;             // 1: the last partition of a (sequence, head tile) merges them all
 };
 
-constexpr int kFusedMaxParts = 16;          // longer splits go to partition_reduce_kernel
+// splits of up to this many partitions merge inside the attention kernel;
+// longer ones go to partition_reduce_kernel (at most 32)
+#ifndef PKV_FUSED_MAX_PARTS
+#define PKV_FUSED_MAX_PARTS 16
+#endif
+constexpr int kFusedMaxParts = PKV_FUSED_MAX_PARTS;
+static_assert(kFusedMaxParts <= 32, "the in-kernel merge keeps one partition per lane");
 
 // The partitions of query heads h0 .. h0 + G - 1 of sequence s, merged by one
 // warp (log-sum-exp, as partition_reduce_kernel) straight from the workspace.
-// The partials were written by other CTAs: read them past L1.
+// Lane L owns D/32 consecutive elements; partial rows are read as vectors, 8
+// partitions at a time in flight.  The partials were written by other CTAs:
+// read them past L1.
 template <int D, int G, typename T>
 __device__ __forceinline__ void merge_partitions_warp(const AttnArgs &a, int s, int h0, int np, int lane) {
+    constexpr int EPL = D / 32;
 #pragma unroll 1
     for (int h = 0; h < G; h++) {
         const size_t base = ((size_t)s * a.num_heads + h0 + h) * a.max_parts;
@@ -416,12 +425,38 @@ __device__ __forceinline__ void merge_partitions_warp(const AttnArgs &a, int s, 
         const float M = warp_max(mp);
         const float wp = lane < np ? exp2f(mp - M) : 0.f;
         const float L = warp_sum(lane < np ? __ldcg(a.ws_l + base + lane) * wp : 0.f);
-        for (int e = lane; e < D; e += 32) {
-            float O = 0.f;
-            for (int p = 0; p < np; p++) O = fmaf(__shfl_sync(kFull, wp, p), __ldcg(a.ws_o + (base + p) * D + e), O);
-            static_cast<T *>(a.out)[((size_t)s * a.num_heads + h0 + h) * D + e] =
-                F16Traits<T>::from_f32(L > 0.f ? O / L : 0.f);
+        float acc[EPL];
+#pragma unroll
+        for (int k = 0; k < EPL; k++) acc[k] = 0.f;
+#pragma unroll 1
+        for (int p0 = 0; p0 < np; p0 += 8) {
+            float ov[8][EPL];
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                const float *src = a.ws_o + (base + p0 + j) * D + lane * EPL;
+                if (p0 + j < np) {
+                    if constexpr (EPL == 4) {
+                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(src));
+                        ov[j][0] = v.x; ov[j][1] = v.y; ov[j][2] = v.z; ov[j][3] = v.w;
+                    } else {
+                        const float2 v = __ldcg(reinterpret_cast<const float2 *>(src));
+                        ov[j][0] = v.x; ov[j][1] = v.y;
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < EPL; k++) ov[j][k] = 0.f;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                const float w = __shfl_sync(kFull, wp, (p0 + j) & 31);
+#pragma unroll
+                for (int k = 0; k < EPL; k++) acc[k] = fmaf(w, ov[j][k], acc[k]);
+            }
         }
+        T *dst = static_cast<T *>(a.out) + ((size_t)s * a.num_heads + h0 + h) * D + lane * EPL;
+#pragma unroll
+        for (int k = 0; k < EPL; k++) dst[k] = F16Traits<T>::from_f32(L > 0.f ? acc[k] / L : 0.f);
     }
 }
 

@@ -243,7 +243,9 @@ def test_launch_count_and_native_library(cuda_device):
     # cache write + attention; three partitions per sequence merge inside the
     # attention kernel (the workspace exists already)
     assert pkv.launch_count() - before == 2
-    # a split into more than 16 partitions adds the merge kernel
+    # a split into more than 16 partitions adds the merge kernel (the first
+    # such call also grows and prepares the workspace)
+    c.eng.attend(c.q_dev, c.dev, partition_size=32)
     before = pkv.launch_count()
     c.eng.decode(c.q_dev, c.k_dev, c.v_dev, c.dev, partition_size=32)
     pkv.check()
