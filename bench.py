@@ -48,6 +48,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="opt13b", choices=["tiny", "opt13b", "llama7b", "sampling", "longgqa"])
     ap.add_argument("--block-size", type=int, default=16)
+    ap.add_argument("--head-dim", type=int, default=128, choices=[64, 128])
     ap.add_argument("--partition-size", type=int, default=-1)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -58,6 +59,7 @@ def make_workload(args, rank: int) -> workloads.Workload:
     kw = {}
     if args.workload == "llama7b":
         kw["block_size"] = args.block_size
+        kw["head_dim"] = args.head_dim
     w = workloads.by_name(args.workload, **kw)
     if rank:
         w = workloads.by_name(args.workload, seed=w.seed + 7919 * rank, **kw) if args.workload != "tiny" else w
@@ -398,8 +400,12 @@ def run_ours(args, rank: int, world: int):
     peak, peak_src = hbm_peak()
     value = total_bytes / (t_step_max * 1e-3) / 1e9
     attn_gbs = kv_bytes / (t_attn * 1e-3) / 1e9
-    traffic = profile_traffic(args.workload if args.workload != "llama7b" else f"llama7b_B{w.block_size}",
-                              pkv.version())
+    traffic = profile_traffic(args.workload if args.workload != "llama7b"
+                              else f"llama7b_B{w.block_size}_d{w.head_dim}", pkv.version())
+    # the block-size trade-off: slots held by the batch vs tokens stored
+    held = int((-(-plan.context_lens.astype(np.int64) // w.block_size)).sum()) * w.block_size
+    frag = {"slots_held": held, "tokens": int(plan.context_lens.sum()),
+            "internal_fragmentation_pct": 100.0 * (1.0 - plan.context_lens.sum() / held)}
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_step_max, "higher_is_better": True, "scaling": "weak",
@@ -416,6 +422,7 @@ def run_ours(args, rank: int, world: int):
                      "ms_per_launch": t_attn},
         "paged_overhead": {"contiguous_ms": t_contig, "paged_ms": t_attn,
                            "slowdown_pct": 100.0 * (t_attn / t_contig - 1.0)},
+        "block_fill": frag,
         "gpu_launches": launches,
         "clocks": {**clk.summary(), "window": "warm-up + timed + e2e legs"},
         "wall_s_timed_region": wall,

@@ -57,13 +57,15 @@ def test_llama7b_small(cuda_device, B):
     _check(Case(workloads.llama7b(block_size=B, num_seqs=12, max_ctx=1500), cuda_device), what=f"llama7b B={B}")
 
 
-@pytest.mark.parametrize("B", [8, 16, 32])
-def test_llama7b_full_sampled(cuda_device, B):
+@pytest.mark.parametrize("B,d", [(8, 128), (16, 128), (32, 128),
+                                 # the block-size study: small and large blocks, small heads
+                                 (4, 128), (128, 128), (4, 64), (16, 64), (64, 64), (128, 64)])
+def test_llama7b_full_sampled(cuda_device, B, d):
     """The full 256 x uniform[1,4096] batch: all heads of 6 sampled sequences."""
-    w = workloads.llama7b(block_size=B)
+    w = workloads.llama7b(block_size=B, head_dim=d)
     sel = [0, 17, 99, 128, 201, 255]
     c = Case(w, cuda_device, gen_device="cuda", subset=sel)
-    _check(c, what=f"llama7b full B={B}")
+    _check(c, what=f"llama7b full B={B} d={d}")
 
 
 def test_sampling_small(cuda_device):

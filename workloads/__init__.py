@@ -135,17 +135,19 @@ def opt13b(num_seqs: int = 64, seed: int = BASE_SEED * 1000 + 2, max_ctx: int = 
 
 
 def llama7b(block_size: int = 16, num_seqs: int = 256, max_ctx: int = 4096,
-            seed: Optional[int] = None) -> Workload:
+            seed: Optional[int] = None, head_dim: int = 128) -> Workload:
+    """Llama-2-7B layer shapes (32 MHA heads).  head_dim 64 (with the same 32
+    heads) is the small-head variant of the block-size study."""
     if seed is None:
         seed = BASE_SEED * 1000 + 3
     rng = _rng(seed)             # the same contexts for every block size
     ctx = uniform_lengths(rng, 1, max_ctx, num_seqs)
     nb = int(sum(_ceil_div(int(c), block_size) for c in ctx))
-    return Workload(f"llama7b: {num_seqs} seqs, MHA 32x128, B={block_size}, ctx uniform[1,{max_ctx}], f16",
-                    num_seqs=num_seqs, num_heads=32, num_kv_heads=32, head_dim=128,
+    return Workload(f"llama7b: {num_seqs} seqs, MHA 32x{head_dim}, B={block_size}, ctx uniform[1,{max_ctx}], f16",
+                    num_seqs=num_seqs, num_heads=32, num_kv_heads=32, head_dim=head_dim,
                     block_size=block_size, dtype="f16", context_lens=ctx,
                     max_blocks_per_seq=_ceil_div(max_ctx, block_size), num_blocks=nb,
-                    seed=seed + block_size)
+                    seed=seed + block_size + (0 if head_dim == 128 else 1000 * head_dim))
 
 
 def sampling(num_prompts: int = 64, samples: int = 4, prompt_len: int = 512,
