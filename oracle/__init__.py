@@ -6,8 +6,9 @@ library (paged_kv_cache_139_gb300) never imports it, and it imports nothing
 from the library.
 
 Contents:
-  pkv_oracle.c   fp64 attention over the paged cache, the slot-mapped cache
-                 write, the block copy, per-partition statistics and their
+  pkv_oracle.c   fp64 attention over the paged cache (decode: one query
+                 token per sequence; prompt phase: many, causal), the
+                 slot-mapped cache write, the block copy, per-partition statistics and their
                  log-sum-exp merge (built by build.py with gcc).
   allocator.py   the reference ref-counted block allocator.
 
@@ -28,7 +29,7 @@ from .build import LIB, build
 
 __all__ = ["AllocatorOOM", "RefAllocator", "blocks_needed", "kv_bytes_per_token",
            "cache_write", "copy_blocks", "paged_attention", "partition_stats",
-           "merge_partitions", "locate_tokens", "decode16", "bits16", "lib"]
+           "merge_partitions", "paged_prefill", "locate_tokens", "decode16", "bits16", "lib"]
 
 _lib = None
 
@@ -48,6 +49,8 @@ def load(path) -> ctypes.CDLL:
     L.oracle_copy_blocks.argtypes = [_p, _p, _i, _i64, _i]
     L.oracle_paged_attention.argtypes = [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i,
                                          _d, _i, _i, _p, _i]
+    L.oracle_paged_prefill.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i,
+                                       _d, _i, _i, _p, _i]
     L.oracle_partition_stats.argtypes = [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _d,
                                          _i, _i, _i, _i, _i, _p, _p, _p]
     L.oracle_merge_partitions.argtypes = [_p, _p, _p, _i, _i, _p]
@@ -168,6 +171,37 @@ def paged_attention(query, key_cache, value_cache, block_tables, context_lens, d
     _check(lib().oracle_paged_attention(_ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), _ptr(cl),
                                         S, bt.shape[1], B, H, Hkv, d, float(scale), _is_bf16(dtype),
                                         NB, w, nw), "paged_attention")
+    return out
+
+
+def paged_prefill(query, key_cache, value_cache, block_tables, context_lens, query_start, dtype,
+                  scale=None, which=None) -> np.ndarray:
+    """fp64 out[T][H][d] of the prompt phase: new token j of sequence s (the
+    last n_s = query_start[s+1] - query_start[s] tokens of its context)
+    attends every token up to its own position.  `which`: optional list of
+    (token, h) to compute (other rows stay NaN)."""
+    q = bits16(query)
+    kc = np.ascontiguousarray(key_cache if isinstance(key_cache, np.ndarray) else bits16(key_cache))
+    vc = np.ascontiguousarray(value_cache if isinstance(value_cache, np.ndarray) else bits16(value_cache))
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    qs = np.ascontiguousarray(query_start, dtype=np.int32)
+    T, H, d = q.shape
+    NB, Hkv, B, d2 = kc.shape
+    S = cl.shape[0]
+    assert d2 == d and vc.shape == kc.shape and bt.shape[0] == S and qs.shape == (S + 1,)
+    assert int(qs[-1]) == T
+    if scale is None:
+        scale = default_scale(d)
+    out = np.full((T, H, d), np.nan, dtype=np.float64)
+    if which is None:
+        w, nw = None, 0
+    else:
+        wa = np.ascontiguousarray(np.asarray(which, dtype=np.int32).reshape(-1, 2))
+        w, nw = _ptr(wa), wa.shape[0]
+    _check(lib().oracle_paged_prefill(_ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), _ptr(cl), _ptr(qs),
+                                      S, bt.shape[1], B, H, Hkv, d, float(scale), _is_bf16(dtype), NB, w, nw),
+           "paged_prefill")
     return out
 
 

@@ -246,6 +246,75 @@ int oracle_paged_attention(double *out, const uint16_t *query,
     return 0;
 }
 
+/* ---- prompt phase: many query tokens per sequence, causal --------------- */
+
+/* The prompt (prefill) phase ("vLLM & PagedAttention" §II and §V) takes a
+ * sequence's new tokens all at once; with a shared prefix (§VII) those are the
+ * request's own input after prefix blocks that are already cached.  Sequence
+ * s has n_s = query_start[s+1] - query_start[s] new tokens, the last n_s of
+ * its context_lens[s]; their keys and values are already in the cache.  New
+ * token j sits at position p = context_lens[s] - n_s + j and, by the causal
+ * sum of the §I attention equation (t <= i), attends tokens 0..p.
+ *
+ * Layouts: query and out [T][H][d] with T = query_start[S]; query_start [S+1]
+ * non-decreasing from 0.  `which` lists (token, h) pairs to compute (n_which
+ * of them); NULL computes all, and the other rows of out are left untouched.
+ * A sequence with n_s = 0 has no rows.  n_s > context_lens[s] is a bad size. */
+int oracle_paged_prefill(double *out, const uint16_t *query,
+                         const uint16_t *key_cache, const uint16_t *value_cache,
+                         const int32_t *block_tables, const int32_t *context_lens,
+                         const int32_t *query_start, int S, int max_blocks, int B,
+                         int H, int Hkv, int d, double scale, int is_bf16, int NB,
+                         const int32_t *which, int n_which)
+{
+    if (S < 0 || max_blocks < 0 || B <= 0 || H <= 0 || Hkv <= 0 || d <= 0 || H % Hkv)
+        return -1;
+    if (S > 0 && query_start[0] != 0)
+        return -1;
+    int64_t max_ctx = 0;
+    for (int s = 0; s < S; s++) {
+        int64_t n = (int64_t)query_start[s + 1] - query_start[s];
+        if (n < 0 || context_lens[s] < 0 || n > context_lens[s])
+            return -1;
+        int rc = check_row(block_tables + (int64_t)s * max_blocks, max_blocks, B,
+                           context_lens[s], NB);
+        if (rc)
+            return rc;
+        if (context_lens[s] > max_ctx)
+            max_ctx = context_lens[s];
+    }
+    int64_t T = S > 0 ? query_start[S] : 0;
+    double *x = malloc(sizeof(double) * (size_t)(max_ctx > 0 ? max_ctx : 1));
+    if (!x)
+        return -1;
+    int64_t n_rows = which ? n_which : T * H;
+    int s = 0;
+    for (int64_t k = 0; k < n_rows; k++) {
+        int64_t tok = which ? which[2 * k] : k / H;
+        int h = which ? which[2 * k + 1] : (int)(k % H);
+        if (tok < 0 || tok >= T || h < 0 || h >= H) {
+            free(x);
+            return -2;
+        }
+        /* the sequence holding new token `tok` */
+        if (which || tok < query_start[s])
+            s = 0;
+        while (query_start[s + 1] <= tok)
+            s++;
+        int64_t n = (int64_t)query_start[s + 1] - query_start[s];
+        int64_t p = context_lens[s] - n + (tok - query_start[s]);
+        double *o = out + (tok * H + h) * d;
+        double m, l;
+        attend_range(query + (tok * H + h) * d, key_cache, value_cache,
+                     block_tables + (int64_t)s * max_blocks, 0, p + 1, B, Hkv,
+                     h / (H / Hkv), d, scale, is_bf16, &m, &l, o, x);
+        for (int i = 0; i < d; i++)
+            o[i] = l > 0.0 ? o[i] / l : 0.0;
+    }
+    free(x);
+    return 0;
+}
+
 /* ---- split context: per-partition statistics and their merge ------------ */
 
 /* For one (s, h): partition p covers tokens [p*P, min((p+1)*P, ctx)).

@@ -327,6 +327,144 @@ def pin_partition_stats_definition():
 
 # -- sizes from the pages -------------------------------------------------------------
 
+# -- prompt phase (many query tokens per sequence, causal) -------------------------
+
+def _prefill_inputs(ctx, nq, H, Hkv, d, B, dtype, seed, permute=True):
+    """A pool, tables and queries for sequences with context ctx[s] whose last
+    nq[s] tokens are the new ones."""
+    S = len(ctx)
+    mb = max(1, -(-max(ctx) // B))
+    NB = S * mb + 3
+    rng = np.random.default_rng(seed)
+    ids = rng.permutation(NB) if permute else np.arange(NB)
+    bt = ids[:S * mb].astype(np.int32).reshape(S, mb)
+    qs = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+    q = _rand16((int(qs[-1]), H, d), dtype, seed + 1)
+    kc = _rand16((NB, Hkv, B, d), dtype, seed + 2)
+    vc = _rand16((NB, Hkv, B, d), dtype, seed + 3)
+    return q, kc, vc, bt, np.array(ctx), qs
+
+
+def _sdpa_causal(q, kc, vc, bt, ctx, qs, H, Hkv):
+    """Textbook masked attention (torch's scaled_dot_product_attention, fp64)
+    over each sequence's tokens copied out in logical order; new token j of
+    sequence s may see tokens t <= ctx[s] - n_s + j."""
+    _, _, B, d = kc.shape
+    G = H // Hkv
+    out = np.zeros((q.shape[0], H, d))
+    for s in range(len(ctx)):
+        n, c = int(qs[s + 1] - qs[s]), int(ctx[s])
+        if n == 0:
+            continue
+        rows = [kc[bt[s, t // B], :, t % B] for t in range(c)]
+        k = torch.stack(rows, 1).to(torch.float64).repeat_interleave(G, dim=0)      # [H][c][d]
+        v = torch.stack([vc[bt[s, t // B], :, t % B] for t in range(c)], 1).to(torch.float64)
+        v = v.repeat_interleave(G, dim=0)
+        qq = q[qs[s]:qs[s + 1]].to(torch.float64).permute(1, 0, 2)                  # [H][n][d]
+        mask = torch.arange(c)[None, :] <= (c - n + torch.arange(n))[:, None]       # [n][c]
+        o = F.scaled_dot_product_attention(qq[None], k[None], v[None], attn_mask=mask)[0]
+        out[qs[s]:qs[s + 1]] = o.permute(1, 0, 2).numpy()
+    return out
+
+
+def pin_prefill_vs_sdpa_causal():
+    """Causal prompt-phase attention equals the library's masked attention on
+    the same tokens: plain prompts (context = new tokens), prompts after a
+    cached prefix, single new tokens and sequences with none."""
+    for dtype, H, Hkv, d, B, ctx, nq in (
+            (torch.float16, 4, 4, 16, 4, (7, 9, 30, 5, 12), (7, 2, 30, 1, 0)),
+            (torch.bfloat16, 8, 2, 32, 8, (40, 17, 64), (13, 17, 40))):
+        q, kc, vc, bt, cl, qs = _prefill_inputs(ctx, nq, H, Hkv, d, B, dtype, 61)
+        got = oracle.paged_prefill(q, kc, vc, bt, cl, qs, dtype)
+        want = _sdpa_causal(q, kc, vc, bt, cl, qs, H, Hkv)
+        assert np.allclose(got, want, rtol=1e-12, atol=1e-14), np.abs(got - want).max()
+
+
+def pin_prefill_rows_are_truncated_decodes():
+    """New token j of sequence s is the decode of a sequence whose context
+    stops at its own position (bit-identical: the same sum over the same
+    tokens)."""
+    H, Hkv, d, B = 4, 2, 16, 4
+    ctx, nq = (21, 8, 13), (6, 8, 1)
+    q, kc, vc, bt, cl, qs = _prefill_inputs(ctx, nq, H, Hkv, d, B, torch.float16, 71)
+    got = oracle.paged_prefill(q, kc, vc, bt, cl, qs, "f16")
+    for s in range(len(ctx)):
+        for j in range(nq[s]):
+            tok = qs[s] + j
+            pos = ctx[s] - nq[s] + j
+            want = oracle.paged_attention(q[tok:tok + 1], kc, vc, bt[s:s + 1], np.array([pos + 1]), "f16")
+            assert np.array_equal(got[tok], want[0]), (s, j)
+
+
+def pin_prefill_prompt_worked_example():
+    """The 7-token prompt of the pages' request walk-through, written into
+    physical blocks 7 and 1: with all scores equal, token i averages values
+    0..i (hand-computed in the fixture)."""
+    g = golden("prefill_prompt_fig6.json")
+    B, n, d, NB = g["block_size"], g["prompt_tokens"], g["head_dim"], g["num_blocks"]
+    kc = np.zeros((NB, 1, B, d), np.uint16)
+    vc = np.zeros((NB, 1, B, d), np.uint16)
+    key = _rand16((n, 1, d), torch.float16, 81)
+    value = torch.tensor([[[t + 1.0, -2.0 * (t + 1)]] for t in range(n)], dtype=torch.float16)
+    blocks = g["physical_blocks"]
+    slots = np.array([blocks[t // B] * B + t % B for t in range(n)])
+    oracle.cache_write(key, value, kc, vc, slots)
+    bt = np.array([blocks], np.int32)
+    q = torch.zeros(n, 1, d, dtype=torch.float16)
+    got = oracle.paged_prefill(q, kc, vc, bt, np.array([n]), np.array([0, n]), "f16")[:, 0]
+    assert np.allclose(got, np.array(g["expected_out_per_token"]), rtol=1e-14, atol=1e-14), got
+
+
+def pin_prefill_future_tokens_ignored():
+    """Changing the keys and values after a token's position leaves its row
+    bit-identical; changing its own key and value changes it."""
+    H, d, B = 2, 8, 4
+    ctx, nq = (19,), (11,)
+    q, kc, vc, bt, cl, qs = _prefill_inputs(ctx, nq, H, H, d, B, torch.float16, 91)
+    kb, vb = oracle.bits16(kc), oracle.bits16(vc)
+    a = oracle.paged_prefill(q, kb, vb, bt, cl, qs, "f16")
+    pos = 12                                     # new token j = 4 sits at position 8 + 4
+    j = pos - (ctx[0] - nq[0])
+    kb2, vb2 = kb.copy(), vb.copy()
+    for t in range(pos + 1, ctx[0]):
+        kb2[bt[0, t // B], :, t % B] ^= 0x1234
+        vb2[bt[0, t // B], :, t % B] ^= 0x0F0F
+    b = oracle.paged_prefill(q, kb2, vb2, bt, cl, qs, "f16")
+    assert np.array_equal(a[:j + 1], b[:j + 1])
+    assert not np.array_equal(a[j + 1:], b[j + 1:])
+    vb3 = vb.copy()
+    vb3[bt[0, pos // B], :, pos % B] ^= 0x0100
+    c = oracle.paged_prefill(q, kb, vb3, bt, cl, qs, "f16")
+    assert np.array_equal(a[:j], c[:j]) and not np.array_equal(a[j], c[j])
+
+
+def pin_prefill_identical_keys_prefix_mean():
+    """All keys equal, after a 10-token prefix: new token j averages the
+    values of tokens 0..10+j (closed form)."""
+    H, d, B = 1, 8, 4
+    ctx, nq = (16,), (6,)
+    q, kc, vc, bt, cl, qs = _prefill_inputs(ctx, nq, H, H, d, B, torch.bfloat16, 101)
+    kb = np.zeros(kc.shape, np.uint16)
+    kb[:] = oracle.bits16(_rand16((d,), torch.bfloat16, 102))
+    got = oracle.paged_prefill(q, kb, vc, bt, cl, qs, "bf16")[:, 0]
+    vals = oracle.decode16(oracle.bits16(vc), "bf16")
+    toks = np.array([vals[bt[0, t // B], 0, t % B] for t in range(ctx[0])])
+    for j in range(nq[0]):
+        assert np.allclose(got[j], toks[:10 + j + 1].mean(axis=0), rtol=1e-13, atol=1e-15)
+
+
+def pin_prefill_which_subset():
+    """Rows asked for by (token, head) equal the same rows of the full run."""
+    ctx, nq = (9, 30, 4), (3, 20, 4)
+    q, kc, vc, bt, cl, qs = _prefill_inputs(ctx, nq, 4, 2, 16, 8, torch.float16, 111)
+    full = oracle.paged_prefill(q, kc, vc, bt, cl, qs, "f16")
+    which = [(26, 3), (0, 0), (22, 1), (5, 2), (3, 0)]
+    part = oracle.paged_prefill(q, kc, vc, bt, cl, qs, "f16", which=which)
+    for t, h in which:
+        assert np.array_equal(part[t, h], full[t, h])
+    assert np.isnan(part[1, 1]).all()
+
+
 def pin_kv_size():
     g = golden("kv_size_opt13b.json")
     per = oracle.kv_bytes_per_token(g["hidden"], g["layers"], g["bytes_per_number"])

@@ -35,6 +35,13 @@ MUTANTS = [
     ("merge ignores partition weight", "L += l[p] * w;", "L += l[p];", 0),
     ("partition end off by one", "int64_t t1 = t0 + P < ctx ? t0 + P : ctx;",
      "int64_t t1 = t0 + P < ctx ? t0 + P - 1 : ctx;", 0),
+    ("prefill own token not attended", "0, p + 1, B, Hkv,", "0, p, B, Hkv,", 0),
+    ("prefill prefix ignored", "int64_t p = context_lens[s] - n + (tok - query_start[s]);",
+     "int64_t p = tok - query_start[s];", 0),
+    ("prefill sequence search off by one", "while (query_start[s + 1] <= tok)", "while (query_start[s + 1] < tok)", 0),
+    ("prefill gqa map modulo", "h / (H / Hkv), d, scale, is_bf16, &m, &l, o, x);",
+     "h % Hkv, d, scale, is_bf16, &m, &l, o, x);", 0),
+    ("prefill no normalisation", "o[i] = l > 0.0 ? o[i] / l : 0.0;", "o[i] = l > 0.0 ? o[i] : 0.0;", 1),
     ("max not tracked", "if (x[t - t0] > m)\n            m = x[t - t0];", "if (x[t - t0] > m)\n            m = 0.0;", 0),
 ]
 
