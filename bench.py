@@ -9,7 +9,11 @@ sum over sequences of context_len x 2 x kv_heads x head_dim x 2 bytes,
 divided by the step time.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload opt13b]
-                    [--block-size B] [--partition-size P] [--impl reference]
+                    [--block-size B] [--head-dim D] [--partition-size P] [--impl reference]
+
+--workload prefix times the prompt phase instead: after a shared cached
+prefix, the copy-on-write of its last block, the cache write of every
+request's own tokens and causal prompt-phase attention, in TFLOP/s.
 
 Prints one JSON line (rank 0).  Under torchrun each rank runs an independent
 replica (a different seed) on its own GPU; the value is all ranks' bytes over
@@ -36,7 +40,9 @@ sys.path.insert(0, str(ROOT))
 import workloads  # noqa: E402
 
 METRIC = "paged decode attention effective KV-read GB/s and % of GB300 HBM peak"
+PREFILL_METRIC = "prompt-phase paged attention TFLOP/s (causal, after a shared prefix)"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 512 << 20
 
 
@@ -46,7 +52,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="opt13b", choices=["tiny", "opt13b", "llama7b", "sampling", "longgqa"])
+    ap.add_argument("--workload", default="opt13b",
+                    choices=["tiny", "opt13b", "llama7b", "sampling", "longgqa", "prefix"])
     ap.add_argument("--block-size", type=int, default=16)
     ap.add_argument("--head-dim", type=int, default=128, choices=[64, 128])
     ap.add_argument("--partition-size", type=int, default=-1)
@@ -81,6 +88,20 @@ def hbm_peak():
         except (ValueError, TypeError):
             pass
     return FALLBACK_HBM_GBS, "fallback"
+
+
+def tensor_peak():
+    """Dense 16-bit tensor peak for a kernel timed alone (TFLOP/s)."""
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            d = json.loads(p.read_text())
+            for k in ("bf16_tflops", "bf16_TFLOPs", "bf16"):
+                if k in d and d[k]:
+                    return float(d[k]), "measured"
+        except (ValueError, TypeError):
+            pass
+    return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def profile_traffic(workload_name: str, version: int):
@@ -179,6 +200,8 @@ def run_reference(args, rank: int, world: int):
     if rank != 0:
         return
     w = make_workload(args, 0)
+    if w.query_lens is not None:
+        return run_reference_prefill(args, w)
     t = workloads.tensors(w, "cpu")
     import oracle
     ref = oracle.RefAllocator(w.num_blocks, w.block_size, workloads.free_order(w.num_blocks, w.seed))
@@ -441,6 +464,215 @@ def run_ours(args, rank: int, world: int):
     print(json.dumps(line), flush=True)
 
 
+# -- prompt phase after a shared prefix --------------------------------------------------
+
+def prefill_flops(ctx: np.ndarray, n: np.ndarray, H: int, d: int) -> float:
+    """Algorithmic FLOPs of causal prompt-phase attention: new token j of a
+    sequence (position ctx - n + j) sees ctx - n + j + 1 keys, each costing
+    2d for q.k and 2d for the weighted value, per query head."""
+    ctx = ctx.astype(np.float64)
+    n = n.astype(np.float64)
+    keys = n * (ctx - n + 1) + n * (n - 1) / 2
+    return float(4.0 * d * H * keys.sum())
+
+
+def prefill_cpu_baseline(w, t, tables, ctx, qs, cached_slots, pairs, slots, budget_s=12.0):
+    import oracle
+    shape = (w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim)
+    kc = np.zeros(shape, np.uint16)
+    vc = np.zeros(shape, np.uint16)
+    oracle.cache_write(t["prefix_key"], t["prefix_value"], kc, vc, cached_slots)
+    if len(pairs):
+        oracle.copy_blocks(kc, pairs)
+        oracle.copy_blocks(vc, pairs)
+    oracle.cache_write(t["key"], t["value"], kc, vc, slots)
+    q = t["query"].cpu()
+    rng = np.random.default_rng(w.seed)
+    T = int(qs[-1])
+    seq_of = np.repeat(np.arange(w.num_seqs), np.diff(qs))
+    flops, rows, t0 = 0.0, 0, time.perf_counter()
+    while time.perf_counter() - t0 < budget_s:
+        tok = int(rng.integers(T))
+        which = [(tok, h) for h in range(w.num_heads)]
+        oracle.paged_prefill(q, kc, vc, tables, ctx, qs, w.dtype, which=which)
+        s = seq_of[tok]
+        pos = int(ctx[s]) - int(qs[s + 1] - qs[s]) + (tok - int(qs[s]))
+        flops += 4.0 * w.head_dim * w.num_heads * (pos + 1)
+        rows += w.num_heads
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": f"{rows} (token, head) rows of {T * w.num_heads} (random new tokens, all heads), fp64, "
+                      f"single thread, {dt:.1f} s"}
+
+
+def run_reference_prefill(args, w):
+    """The oracle's prompt-phase attention, as it stands, on bounded samples of
+    the shared-prefix workload (same allocator plan as our arm)."""
+    import oracle
+    B = w.block_size
+    ref = oracle.RefAllocator(w.num_blocks, B, workloads.free_order(w.num_blocks, w.seed))
+    root = ref.seq_new(w.prefix_len)
+    rt = ref.block_table(root)
+    cached = np.array([rt[i // B] * B + i % B for i in range(w.prefix_len)], np.int64)
+    kids = [ref.fork(root) for _ in range(w.num_seqs)]
+    slots, pairs = ref.append_batch(np.repeat(np.asarray(kids, np.int32), w.query_lens))
+    tables = np.full((w.num_seqs, w.max_blocks_per_seq), -1, np.int32)
+    for i, k in enumerate(kids):
+        bt = ref.block_table(k)
+        tables[i, :len(bt)] = bt
+    ctx = np.array([ref.seq_len(k) for k in kids], np.int32)
+    qs = np.concatenate([[0], np.cumsum(w.query_lens)]).astype(np.int32)
+    t = workloads.prefill_tensors(w, "cpu")
+    per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    vals = []
+    for i in range(args.warmup + args.steps):
+        cb = prefill_cpu_baseline(w, t, tables, ctx, qs, cached, pairs, np.asarray(slots, np.int64),
+                                  budget_s=per_step)
+        if i >= args.warmup:
+            vals.append(cb)
+    v = statistics.median([c["value"] for c in vals])
+    flops = prefill_flops(ctx, w.query_lens, w.num_heads, w.head_dim)
+    line = {"impl": "reference", "metric": PREFILL_METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": flops / (v * 1e12) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {**w.describe(), "prefix_len": w.prefix_len,
+                                            "kernel": "oracle (fp64 C, CPU)"},
+            "cpu_baseline": {**vals[-1], "value": v},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def run_prefill(args, rank: int, world: int):
+    """One step: the copy-on-write copies of the shared prefix's last block,
+    the cache write of every request's own tokens, and prompt-phase attention
+    of those tokens over the paged cache."""
+    import paged_kv_cache_139_gb300 as pkv
+    from paged_kv_cache_139_gb300.engine import PagedKVCache
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w = make_workload(args, rank)
+    t = workloads.prefill_tensors(w, device=dev)
+    eng = PagedKVCache(w.num_blocks, w.num_kv_heads, w.head_dim, w.block_size, w.torch_dtype, dev,
+                       w.max_blocks_per_seq, workloads.free_order(w.num_blocks, w.seed))
+    B = w.block_size
+    root = eng.new_sequence(w.prefix_len)
+    rt = eng.alloc.block_table(root)
+    cached_slots = np.array([rt[i // B] * B + i % B for i in range(w.prefix_len)], np.int64)
+    eng.write(t["prefix_key"], t["prefix_value"], torch.from_numpy(cached_slots).to(dev))
+    kids = [eng.fork(root) for _ in range(w.num_seqs)]
+    plan = eng.plan_prefill(kids, w.query_lens)
+    step = eng.upload_prefill(plan)
+    q, key, value = t["query"], t["key"], t["value"]
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flops = prefill_flops(plan.context_lens, np.diff(plan.query_start), w.num_heads, w.head_dim)
+    T = int(plan.query_start[-1])
+    prep = eng.prepare_prefill(q, key, value, step, out)
+
+    clk = ClockSampler(dev.index).__enter__()
+    t_w, n_w = time.perf_counter(), 0
+    while n_w < args.warmup or time.perf_counter() - t_w < 1.0:
+        flush.zero_()
+        prep()
+        n_w += 1
+        if n_w % 16 == 0:
+            torch.cuda.synchronize(dev)
+    pkv.check()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = pkv.launch_count()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        prep.copy()
+        prep.write()
+        ev[i][1].record(stream)
+        prep.attend()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    if dist:
+        dist.barrier()
+    launches = pkv.launch_count() - launches0
+    pkv.check()
+    t_step = statistics.fmean(a.elapsed_time(c) for a, _, c in ev)
+    t_attn = statistics.fmean(b.elapsed_time(c) for _, b, c in ev)
+    t_front = statistics.fmean(a.elapsed_time(b) for a, b, _ in ev)
+
+    e2e = None
+    if not args.no_e2e:
+        h = {n: x.cpu().pin_memory() for n, x in (("q", q), ("key", key), ("value", value))}
+        h["slots"] = torch.from_numpy(plan.slots).pin_memory()
+        h["tables"] = torch.from_numpy(plan.tables).pin_memory()
+        h["ctx"] = torch.from_numpy(plan.context_lens).pin_memory()
+        h["qs"] = torch.from_numpy(plan.query_start).pin_memory()
+        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        d = {n: torch.empty_like(x, device=dev) for n, x in h.items()}
+        dstep = type(step)(d["slots"], step.pairs, d["tables"], d["ctx"], d["qs"], step.max_query_len)
+        eprep = eng.prepare_prefill(d["q"], d["key"], d["value"], dstep, out)
+        h2d = sum(x.numel() * x.element_size() for x in h.values())
+        d2h = h_out.numel() * h_out.element_size()
+        times = []
+        for i in range(args.warmup + args.steps):
+            flush.zero_()
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            for n in h:
+                d[n].copy_(h[n], non_blocking=True)
+            eprep()
+            h_out.copy_(out, non_blocking=True)
+            torch.cuda.synchronize(dev)
+            if i >= args.warmup:
+                times.append(time.perf_counter() - t0)
+        t_e2e = statistics.fmean(times)
+        e2e = {"value": flops / t_e2e / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3}
+        pkv.check()
+    clk.__exit__(None, None, None)
+    t_step_max, total_flops = aggregate(t_step, flops, dist, dev)
+    if rank != 0:
+        return
+    peak, peak_src = tensor_peak()
+    achieved = flops / (t_attn * 1e-3) / 1e12
+    esz = 2
+    write_bytes = 2 * 2 * T * w.num_kv_heads * w.head_dim * esz + 8 * T
+    copy_bytes = 2 * 2 * len(plan.pairs) * w.num_kv_heads * B * w.head_dim * esz
+    line = {
+        "metric": PREFILL_METRIC, "value": total_flops / (t_step_max * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "kv_dtype": w.dtype,
+        "data": "synthetic",
+        "config": {**w.describe(), "prefix_len": w.prefix_len, "new_tokens": T,
+                   "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB memset, outside the timed events)",
+                   "flops_per_step": flops, "parallelism": f"replicas x{world}"},
+        "tokens_per_s": T * world / (t_step_max * 1e-3),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": profile_traffic("prefix", pkv.version()),
+                     "kernel": "paged_attention_prefill (tcgen05, TMEM accumulators)",
+                     "peak_source": f"{peak_src} {'MEASURED_PEAKS.json bf16_tflops' if peak_src == 'measured' else '1.9 PFLOP/s bf16 burst'}",
+                     "ms_per_launch": t_attn},
+        "write_and_copy": {"ms": t_front, "copy_pairs": int(len(plan.pairs)), "bytes": write_bytes + copy_bytes,
+                           "gbs": (write_bytes + copy_bytes) / (t_front * 1e-3) / 1e9},
+        "gpu_launches": launches,
+        "clocks": {**clk.summary(), "window": "warm-up + timed + e2e legs"},
+        "wall_s_timed_region": wall,
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline:
+        tc = workloads.prefill_tensors(w, "cpu")
+        line["cpu_baseline"] = prefill_cpu_baseline(w, tc, plan.tables, plan.context_lens, plan.query_start,
+                                                    cached_slots, plan.pairs, plan.slots)
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", 0))
@@ -451,6 +683,8 @@ def main():
         dist.init_process_group("nccl")
     if args.impl == "reference":
         run_reference(args, rank, world)
+    elif args.workload == "prefix":
+        run_prefill(args, rank, world)
     else:
         run_ours(args, rank, world)
     if world > 1 and args.impl == "ours":

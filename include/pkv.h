@@ -160,6 +160,48 @@ pkv_status paged_attention_decode_noalloc(void *out_dev, const void *query_dev,
                                           int partition_size, pkv_dtype dtype,
                                           struct CUstream_st *stream);
 
+/* ---------------------------------------------------------------------------
+ * paged_attention_prefill -- attention of the prompt phase over the paged
+ * cache: many new tokens per sequence, causal, after an optional cached
+ * prefix ("vLLM & PagedAttention", §I attention equation with its sum over
+ * t <= i; §II and §V, the prompt phase; §VII, a shared prefix whose blocks
+ * are already cached, so that only the request's own input is computed).
+ *
+ * Sequence s has n_s = query_start[s+1] - query_start[s] new tokens, the
+ * last n_s of its context_lens[s] tokens; their keys and values must already
+ * be in the cache (kv_reshape_and_cache first).  New token j of sequence s,
+ * row i = query_start[s] + j of query and out, sits at position
+ * p = context_lens[s] - n_s + j and gives, for every query head h
+ * (kv head g = h / (num_heads / num_kv_heads)):
+ *   x_t = scale * query[i][h] . K_t  for t = 0..p   (K_t, V_t as above)
+ *   out[i][h] = sum_{t<=p} softmax(x)_t * V_t, rounded to `dtype`.
+ * n_s = context_lens[s] is a plain prompt; n_s = 1 is one decode step.
+ *
+ *   out_dev, query_dev  [num_tokens][num_heads][head_dim], 16-byte aligned;
+ *                       num_tokens = query_start[num_seqs].
+ *   query_start_dev     int32 [num_seqs + 1], query_start[0] = 0,
+ *                       non-decreasing.  A sequence with n_s < 0,
+ *                       n_s > context_lens[s], a context beyond its table
+ *                       row or query_start[s+1] > num_tokens latches
+ *                       PKV_EINDEX and writes none of its rows.
+ *   max_query_len       host-side bound on every n_s (0 = num_tokens); it
+ *                       sizes the grid, so a larger n_s leaves rows unwritten.
+ *   num_blocks          table entries outside [0, num_blocks) latch
+ *                       PKV_EINDEX (the call reads block 0 instead).
+ * No workspace: the call allocates nothing.  num_seqs <= 65535; head_dim in
+ * {64, 128}; block_size a power of two in [4, 128]; num_heads % num_kv_heads
+ * == 0.  Asynchronous on `stream`; PKV_EINVAL for bad arguments, launching
+ * nothing.
+ * ------------------------------------------------------------------------- */
+pkv_status paged_attention_prefill(void *out_dev, const void *query_dev,
+                                   const void *key_cache_dev, const void *value_cache_dev,
+                                   const int32_t *block_tables_dev,
+                                   const int32_t *context_lens_dev,
+                                   const int32_t *query_start_dev, int num_seqs, int num_tokens,
+                                   int max_query_len, int max_blocks_per_seq, int block_size,
+                                   int num_blocks, int num_heads, int num_kv_heads, int head_dim,
+                                   float scale, pkv_dtype dtype, struct CUstream_st *stream);
+
 /* Bytes of workspace paged_attention_decode needs for these sizes: 256 for
  * the counters, plus the partition partials when a context can span more
  * than one partition.  partition_size as above. */

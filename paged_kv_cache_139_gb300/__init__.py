@@ -24,7 +24,8 @@ import torch
 from ._lib import STATUS, load
 
 __all__ = ["PkvError", "PkvOOM", "kv_reshape_and_cache", "paged_attention_decode",
-           "paged_attention_decode_noalloc", "paged_attention_workspace_size", "make_workspace",
+           "paged_attention_decode_noalloc", "paged_attention_prefill", "paged_attention_workspace_size",
+           "make_workspace",
            "paged_attention_partition_size", "copy_blocks",
            "validate_copy_pairs", "check", "launch_count", "version", "BlockAllocator", "library_path"]
 
@@ -176,6 +177,36 @@ def paged_attention_decode(out: torch.Tensor, query: torch.Tensor, key_cache: to
         S, mb, max_context_len, B, NB, H, Hkv, d, float(scale), partition_size, ws_ptr, ws_bytes,
         _dtype_code(query), _stream(stream, query.device))
     _ck(rc, "paged_attention_decode")
+    return out
+
+
+def paged_attention_prefill(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                            value_cache: torch.Tensor, block_tables: torch.Tensor,
+                            context_lens: torch.Tensor, query_start: torch.Tensor,
+                            scale: Optional[float] = None, max_query_len: int = 0,
+                            stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Prompt-phase attention: out/query [T][H][d] hold the new tokens of all
+    sequences back to back, query_start int32 [S+1] their offsets; the new
+    tokens of sequence s are the last n_s of its context_lens[s] and each
+    attends every token up to its own position.  Their keys and values must
+    already be in the cache.  Returns out."""
+    T, H, d = query.shape
+    NB, Hkv, B, d2 = key_cache.shape
+    S = context_lens.shape[0]
+    if d2 != d or out.shape != query.shape or value_cache.shape != key_cache.shape:
+        raise ValueError("paged_attention_prefill: shape mismatch")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or query_start.shape != (S + 1,):
+        raise ValueError("paged_attention_prefill: block_tables must be [S][max_blocks], query_start [S+1]")
+    if not (query.dtype == out.dtype == key_cache.dtype == value_cache.dtype):
+        raise TypeError("paged_attention_prefill: dtype mismatch")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    rc = load().paged_attention_prefill(
+        _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
+        _dev(block_tables, "block_tables", torch.int32), _dev(context_lens, "context_lens", torch.int32),
+        _dev(query_start, "query_start", torch.int32), S, T, max_query_len, block_tables.shape[1], B, NB, H, Hkv,
+        d, float(scale), _dtype_code(query), _stream(stream, query.device))
+    _ck(rc, "paged_attention_prefill")
     return out
 
 

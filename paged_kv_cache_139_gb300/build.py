@@ -17,7 +17,7 @@ OBJ = PKG / "_build"
 LIBDIR = PKG / "lib"
 LIB = LIBDIR / "libpkv.so"
 
-CUDA_SOURCES = ["runtime.cu", "cache_ops.cu", "attention.cu", "attention_noalloc.cu"]
+CUDA_SOURCES = ["runtime.cu", "cache_ops.cu", "attention.cu", "attention_noalloc.cu", "prefill.cu"]
 CXX_SOURCES = ["allocator.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -36,6 +36,7 @@
 #include <type_traits>
 
 #include "pkv_host.cuh"
+#include "pkv_tmap.h"
 
 namespace pkv {
 namespace {
@@ -1262,32 +1263,13 @@ __global__ void workspace_magic_kernel(WsHeader *h) {
 }
 
 // cuTensorMapEncodeTiled from the driver, looked up once.
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static std::once_flag once;
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
 // The cache [NB][Hkv][B][D] as a 4-D tensor (innermost first); a box is 64
 // elements of d by min(B, 32) tokens of one (block, kv head), 128-byte swizzle.
 bool encode_cache_map(CUtensorMap *map, const void *base, int num_blocks, int Hkv, int B, int D, bool bf16) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-    if (!enc) return false;
     const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)B, (cuuint64_t)Hkv, (cuuint64_t)(num_blocks > 0 ? num_blocks : 1)};
     const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)B * D * 2, (cuuint64_t)Hkv * B * D * 2};
     const cuuint32_t box[4] = {64u, (cuuint32_t)(B < kStageRows ? B : kStageRows), 1u, 1u};
-    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-    return enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
-               const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return encode_tiled16(map, base, 4, dims, strides, box, bf16);
 }
 
 template <int D, int G, typename T, bool MMA>

@@ -20,7 +20,7 @@ import ctypes
 import math
 
 from . import (BlockAllocator, PkvError, copy_blocks, kv_reshape_and_cache, make_workspace,
-               paged_attention_decode, paged_attention_workspace_size)
+               paged_attention_decode, paged_attention_prefill, paged_attention_workspace_size)
 from ._lib import load
 
 
@@ -44,6 +44,28 @@ class DeviceStep:
     tables: torch.Tensor
     context_lens: torch.Tensor
     max_context_len: int
+
+
+@dataclasses.dataclass
+class PrefillPlan:
+    """Host-side result of allocating the new tokens of a prompt-phase step."""
+
+    seqs: np.ndarray          # int32 [n]
+    slots: np.ndarray         # int64 [T], sequence-major
+    pairs: np.ndarray         # int32 [m][2] copy-on-write (src, dst)
+    tables: np.ndarray        # int32 [n][max_blocks]
+    context_lens: np.ndarray  # int32 [n]
+    query_start: np.ndarray   # int32 [n + 1]
+
+
+@dataclasses.dataclass
+class DevicePrefill:
+    slots: torch.Tensor
+    pairs: torch.Tensor
+    tables: torch.Tensor
+    context_lens: torch.Tensor
+    query_start: torch.Tensor
+    max_query_len: int
 
 
 class PagedKVCache:
@@ -85,6 +107,27 @@ class PagedKVCache:
         s = np.asarray(seqs, dtype=np.int32)
         tables, ctx = self.alloc.build_block_tables(s, self.max_blocks_per_seq)
         return StepPlan(s, np.empty(0, np.int64), np.empty((0, 2), np.int32), tables, ctx)
+
+    def plan_prefill(self, seqs: Sequence[int], new_tokens: Sequence[int]) -> PrefillPlan:
+        """Append new_tokens[i] tokens to seqs[i] (all or nothing): the prompt
+        phase of a request, or its own input after a forked shared prefix."""
+        s = np.asarray(seqs, dtype=np.int32)
+        n = np.asarray(new_tokens, dtype=np.int64)
+        slots, pairs = self.alloc.append_batch(np.repeat(s, n).astype(np.int32))
+        tables, ctx = self.alloc.build_block_tables(s, self.max_blocks_per_seq)
+        qs = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+        return PrefillPlan(s, slots, pairs, tables, ctx, qs)
+
+    def upload_prefill(self, plan: PrefillPlan, non_blocking: bool = False) -> DevicePrefill:
+        d = self.device
+        n = np.diff(plan.query_start)
+        return DevicePrefill(
+            slots=torch.from_numpy(plan.slots).to(d, non_blocking=non_blocking),
+            pairs=torch.from_numpy(np.ascontiguousarray(plan.pairs)).to(d, non_blocking=non_blocking),
+            tables=torch.from_numpy(plan.tables).to(d, non_blocking=non_blocking),
+            context_lens=torch.from_numpy(plan.context_lens).to(d, non_blocking=non_blocking),
+            query_start=torch.from_numpy(plan.query_start).to(d, non_blocking=non_blocking),
+            max_query_len=int(n.max()) if n.size else 0)
 
     def upload(self, plan: StepPlan, non_blocking: bool = False) -> DeviceStep:
         d = self.device
@@ -130,6 +173,26 @@ class PagedKVCache:
         self.copy_on_write(step.pairs)
         self.write(key, value, step.slots)
         return self.attend(query, step, out, scale, partition_size)
+
+    def prefill(self, query: torch.Tensor, key: torch.Tensor, value: torch.Tensor, step: DevicePrefill,
+                out: Optional[torch.Tensor] = None, scale: Optional[float] = None) -> torch.Tensor:
+        """The device half of a prompt-phase step: copy-on-write copies (a
+        shared prefix's partly filled last block), the new tokens' cache write,
+        then causal attention of the new tokens over the paged cache."""
+        if out is None:
+            out = torch.empty_like(query)
+        self.copy_on_write(step.pairs)
+        self.write(key, value, step.slots)
+        return paged_attention_prefill(out, query, self.key_cache, self.value_cache, step.tables,
+                                       step.context_lens, step.query_start, scale=scale,
+                                       max_query_len=step.max_query_len)
+
+    def prepare_prefill(self, query: torch.Tensor, key: torch.Tensor, value: torch.Tensor, step: DevicePrefill,
+                        out: torch.Tensor, scale: Optional[float] = None,
+                        stream: Optional[torch.cuda.Stream] = None) -> "PreparedPrefill":
+        """The device calls of a prompt-phase step on fixed buffers, with their
+        C-ABI arguments built once."""
+        return PreparedPrefill(self, query, key, value, step, out, scale, stream)
 
     def prepare(self, query: torch.Tensor, key: torch.Tensor, value: torch.Tensor, step: DeviceStep,
                 out: torch.Tensor, scale: Optional[float] = None, partition_size: int = 0,
@@ -186,6 +249,57 @@ class PreparedStep:
         rc = self._L.paged_attention_decode(*self._attend)
         if rc:
             raise PkvError(rc, "paged_attention_decode")
+
+    def __call__(self) -> None:
+        self.copy()
+        self.write()
+        self.attend()
+
+
+class PreparedPrefill:
+    """copy_blocks, kv_reshape_and_cache and paged_attention_prefill for one
+    set of buffers, their arguments checked and marshalled once."""
+
+    def __init__(self, eng: PagedKVCache, query, key, value, step: DevicePrefill, out, scale, stream):
+        self._L = load()
+        T, H, d = query.shape
+        assert out.shape == query.shape and out.dtype == query.dtype == eng.key_cache.dtype
+        assert key.shape == value.shape == (step.slots.shape[0], eng.num_kv_heads, d)
+        for t in (query, key, value, out, step.slots, step.tables, step.context_lens, step.query_start, step.pairs):
+            assert t.is_cuda and t.is_contiguous()
+        code = 1 if query.dtype == torch.bfloat16 else 0
+        st = ctypes.c_void_p((stream or torch.cuda.current_stream(eng.device)).cuda_stream)
+        self._keep = (query, key, value, step, out)
+        NB, B = eng.num_blocks, eng.block_size
+        block_bytes = eng.num_kv_heads * B * d * eng.key_cache.element_size()
+        n = step.pairs.shape[0] if step.pairs.dim() == 2 else 0
+        self._copy = [(c.data_ptr(), step.pairs.data_ptr(), n, block_bytes, NB, st)
+                      for c in (eng.key_cache, eng.value_cache)] if n else []
+        Tw = step.slots.shape[0]
+        self._write = (key.data_ptr(), value.data_ptr(), eng.key_cache.data_ptr(), eng.value_cache.data_ptr(),
+                       step.slots.data_ptr(), Tw, eng.num_kv_heads, d, B, NB, code, st)
+        S = step.context_lens.shape[0]
+        self._attend = (out.data_ptr(), query.data_ptr(), eng.key_cache.data_ptr(), eng.value_cache.data_ptr(),
+                        step.tables.data_ptr(), step.context_lens.data_ptr(), step.query_start.data_ptr(), S, T,
+                        step.max_query_len, step.tables.shape[1], B, NB, H, eng.num_kv_heads, d,
+                        float(1.0 / math.sqrt(d) if scale is None else scale), code, st)
+
+    def copy(self) -> None:
+        for args in self._copy:
+            rc = self._L.copy_blocks(*args)
+            if rc:
+                raise PkvError(rc, "copy_blocks")
+
+    def write(self) -> None:
+        if self._write[5]:
+            rc = self._L.kv_reshape_and_cache(*self._write)
+            if rc:
+                raise PkvError(rc, "kv_reshape_and_cache")
+
+    def attend(self) -> None:
+        rc = self._L.paged_attention_prefill(*self._attend)
+        if rc:
+            raise PkvError(rc, "paged_attention_prefill")
 
     def __call__(self) -> None:
         self.copy()

@@ -1,0 +1,164 @@
+"""paged_attention_prefill (and the prompt-phase cache write and
+copy-on-write before it) against the oracle, through the C ABI.
+
+Every case builds the batch twice (tests/prefill_cases.py): the allocator
+plans are compared exactly, the K/V pools bit for bit (NaN-filled before the
+writes, so that any read of an unwritten slot would show), and the
+attention rows within the allclose tolerance of the decode tests."""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_139_gb300 as pkv
+import workloads
+from prefill_cases import PrefillCase, assert_rows_close, custom
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(c: PrefillCase, what: str, which=None, pools=True):
+    c.check_allocator()
+    if pools:
+        kc, vc = c.oracle_caches()
+        gk, gv = c.gpu_caches()
+        assert np.array_equal(gk, kc) and np.array_equal(gv, vc), f"{what}: cache pools differ"
+    T, H = c.q_dev.shape[0], c.w.num_heads
+    if which is None:
+        which = [(t, h) for t in range(T) for h in range(H)]
+    want = c.oracle_out(which)
+    got = c.out.double().cpu().numpy()
+    assert_rows_close(got, want, which, what)
+
+
+def test_plain_prompts(cuda_device):
+    """Context = the new tokens: a plain causal prompt, across tile edges."""
+    ctx = (1, 5, 127, 128, 129, 300, 700)
+    _check(PrefillCase(custom(ctx, ctx, H=4, Hkv=4), cuda_device), "plain prompts")
+
+
+def test_prompts_after_cached_tokens(cuda_device):
+    ctx, new = (40, 300, 1030, 2000, 129), (40, 1, 200, 513, 2)
+    _check(PrefillCase(custom(ctx, new, H=8, Hkv=2, d=64, B=8, dtype="bf16"), cuda_device), "after cached tokens")
+
+
+def test_shared_prefix_small(cuda_device):
+    """Five requests fork a 333-token prefix: each copies the prefix's partly
+    filled last block on its first write."""
+    w = custom([333 + n for n in (1, 17, 128, 255, 300)], (1, 17, 128, 255, 300), H=8, Hkv=2, dtype="bf16",
+               prefix_len=333)
+    c = PrefillCase(w, cuda_device)
+    assert len(c.plan.pairs) == 5
+    _check(c, "shared prefix")
+
+
+def test_prefix_ending_on_a_block_boundary(cuda_device):
+    """A 320-token prefix fills whole blocks: nothing is copied."""
+    w = custom([320 + n for n in (3, 200)], (3, 200), prefix_len=320)
+    c = PrefillCase(w, cuda_device)
+    assert len(c.plan.pairs) == 0
+    _check(c, "block-aligned prefix")
+
+
+@pytest.mark.parametrize("B", [4, 8, 16, 32, 64, 128])
+@pytest.mark.parametrize("d", [64, 128])
+def test_block_and_head_sizes(cuda_device, B, d):
+    w = custom((5, 130, 300, 1), (5, 100, 257, 1), H=2, Hkv=1, d=d, B=B, dtype="f16" if B % 8 else "bf16")
+    _check(PrefillCase(w, cuda_device), f"B={B} d={d}")
+
+
+@pytest.mark.parametrize("H,Hkv", [(4, 4), (4, 2), (8, 2), (12, 4), (7, 1), (6, 3)])
+def test_head_groupings(cuda_device, H, Hkv):
+    w = custom((200, 77, 129), (150, 77, 1), H=H, Hkv=Hkv, d=64, dtype="bf16")
+    _check(PrefillCase(w, cuda_device), f"H={H} Hkv={Hkv}")
+
+
+def test_sequences_without_new_tokens(cuda_device):
+    w = custom((50, 10, 300, 7), (20, 0, 130, 0), H=4, Hkv=2)
+    c = PrefillCase(w, cuda_device)
+    _check(c, "empty sequences")
+
+
+def test_single_new_token_matches_decode(cuda_device):
+    """One new token per sequence is a decode step: the prompt-phase kernel
+    and the decode kernel agree (and both match the oracle)."""
+    ctx = (1, 33, 500, 1300)
+    w = custom(ctx, (1, 1, 1, 1), H=8, Hkv=2, dtype="bf16")
+    c = PrefillCase(w, cuda_device)
+    _check(c, "single new token")
+    dec = torch.empty_like(c.q_dev)
+    pkv.paged_attention_decode(dec, c.q_dev, c.eng.key_cache, c.eng.value_cache, c.dev.tables,
+                               c.dev.context_lens)
+    pkv.check()
+    err = (dec.double() - c.out.double()).abs().max().item()
+    assert err < 4e-3, err
+
+
+def test_unwritten_slots_never_weigh(cuda_device):
+    """NaN-filled and zero-filled pools give bit-identical outputs."""
+    w = custom((29, 250, 1001), (29, 250, 130), H=4, Hkv=2, B=16)
+    a = PrefillCase(w, cuda_device, nan_pool=True)
+    b = PrefillCase(w, cuda_device, nan_pool=False)
+    assert torch.isfinite(a.out.float()).all()
+    assert torch.equal(a.out, b.out)
+
+
+def test_placement_invariance(cuda_device):
+    """The same logical blocks at other physical blocks: bit-identical rows."""
+    w = custom((400, 130, 900), (400, 64, 300), H=4, Hkv=4, B=16)
+    a = PrefillCase(w, cuda_device)
+    rev = workloads.free_order(w.num_blocks, w.seed)[::-1].copy()
+    b = PrefillCase(w, cuda_device, order=rev)
+    assert not np.array_equal(a.plan.tables, b.plan.tables)
+    assert torch.equal(a.out, b.out)
+
+
+def test_repeated_calls_are_identical(cuda_device):
+    w = custom((700, 260), (700, 130), H=4, Hkv=2)
+    c = PrefillCase(w, cuda_device)
+    outs = [c.rerun() for _ in range(3)]
+    assert all(torch.equal(c.out, o) for o in outs)
+
+
+def test_prefix_workload_full_sampled(cuda_device):
+    """The 32-request shared-prefix workload (Llama-2-7B layer shapes) in the
+    launch the benchmark times: sampled rows against the oracle."""
+    c = PrefillCase(workloads.prefix(), cuda_device)
+    assert len(c.plan.pairs) == 32
+    _check(c, "prefix workload", which=c.sample_rows(n_per_seq=4))
+
+
+def test_prefix_workload_gqa_bf16_sampled(cuda_device):
+    c = PrefillCase(workloads.prefix(num_kv_heads=8, dtype="bf16", num_requests=16, prefix_len=2050,
+                                     max_own=1024), cuda_device)
+    _check(c, "prefix workload gqa", which=c.sample_rows(n_per_seq=4))
+
+
+def test_bad_context_is_latched(cuda_device):
+    """More new tokens than context: PKV_EINDEX, rows unwritten, and the next
+    call works."""
+    w = custom((300, 40), (300, 40), H=2, Hkv=2)
+    c = PrefillCase(w, cuda_device)
+    bad_ctx = c.dev.context_lens.clone()
+    bad_ctx[1] = 10                                   # 40 new tokens, context 10
+    o = torch.full_like(c.q_dev, 7.0)
+    pkv.paged_attention_prefill(o, c.q_dev, c.eng.key_cache, c.eng.value_cache, c.dev.tables, bad_ctx,
+                                c.dev.query_start, max_query_len=300)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.check()
+    assert e.value.status == 3                        # PKV_EINDEX
+    assert (o[300:] == 7.0).all()
+    assert torch.equal(c.rerun(), c.out)
+
+
+def test_bad_block_is_latched(cuda_device):
+    w = custom((100,), (100,), H=2, Hkv=2)
+    c = PrefillCase(w, cuda_device)
+    t = c.dev.tables.clone()
+    t[0, 2] = w.num_blocks + 5
+    o = torch.empty_like(c.q_dev)
+    pkv.paged_attention_prefill(o, c.q_dev, c.eng.key_cache, c.eng.value_cache, t, c.dev.context_lens,
+                                c.dev.query_start)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.check()
+    assert e.value.status == 3
+    assert torch.equal(c.rerun(), c.out)

@@ -15,6 +15,7 @@ and §VII for parallel sampling over shared prompt blocks):
   llama7b     Llama-2-7B layer (32 x 128 MHA), 256 seqs, uniform[1,4096], B swept
   sampling    64 prompts x 4 samples over shared prompt blocks (CoW)
   longgqa     32 q-heads / 8 kv-heads, 8 seqs x 32768 tokens, bf16
+  prefix      prompt phase: 32 requests after a shared 1000-token prefix
 
 The pages give no length distribution for real traffic (their ShareGPT and
 Alpaca traces are not available here); the lognormal and uniform models below
@@ -54,6 +55,10 @@ class Workload:
     samples_per_prompt: int = 1
     prompt_lens: Optional[np.ndarray] = None   # int64 [num_prompts]
     suffix_lens: Optional[np.ndarray] = None   # int64 [num_seqs]
+    # prompt-phase (shared-prefix) workload only: new tokens per sequence, the
+    # last query_lens[s] of context_lens[s], after a prefix of prefix_len
+    query_lens: Optional[np.ndarray] = None    # int64 [num_seqs]
+    prefix_len: int = 0
 
     @property
     def torch_dtype(self) -> torch.dtype:
@@ -190,9 +195,34 @@ def longgqa(num_seqs: int = 8, ctx_len: int = 32768, seed: int = BASE_SEED * 100
                     num_blocks=num_seqs * mb, seed=seed, partition_size=partition_size)
 
 
+def prefix(num_requests: int = 32, prefix_len: int = 1000, min_own: int = 64, max_own: int = 512,
+           num_heads: int = 32, num_kv_heads: int = 32, head_dim: int = 128, block_size: int = 16,
+           dtype: str = "f16", seed: int = BASE_SEED * 1000 + 6) -> Workload:
+    """Shared prefix ("vLLM & PagedAttention" §VII): one cached prefix (a
+    system prompt or few-shot examples) of prefix_len tokens and num_requests
+    requests whose own inputs, uniform[min_own, max_own] tokens, follow it.
+    The prompt phase runs over the own tokens only; each attends the prefix
+    and the own tokens up to itself.  The pool holds the prefix once, each
+    request's copy of the prefix's partly filled last block and its new
+    blocks, plus slack."""
+    B = block_size
+    rng = _rng(seed)
+    own = uniform_lengths(rng, min_own, max_own, num_requests)
+    ctx = prefix_len + own
+    shared_full = prefix_len // B
+    nb = _ceil_div(prefix_len, B) + int(sum(_ceil_div(int(c), B) - shared_full for c in ctx)) + 64
+    return Workload(f"prefix: {num_requests} requests after a shared {prefix_len}-token prefix, own input "
+                    f"uniform[{min_own},{max_own}], {'MHA' if num_heads == num_kv_heads else 'GQA'} "
+                    f"{num_heads}/{num_kv_heads}x{head_dim}, B={B}, {dtype}",
+                    num_seqs=num_requests, num_heads=num_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
+                    block_size=B, dtype=dtype, context_lens=ctx,
+                    max_blocks_per_seq=_ceil_div(prefix_len + max_own, B), num_blocks=nb, seed=seed,
+                    query_lens=own, prefix_len=prefix_len)
+
+
 def by_name(name: str, **kw) -> Workload:
     table = {"tiny": tiny, "opt13b": opt13b, "llama7b": llama7b,
-             "sampling": sampling, "longgqa": longgqa}
+             "sampling": sampling, "longgqa": longgqa, "prefix": prefix}
     return table[name](**kw)
 
 
@@ -214,6 +244,24 @@ def tensors(w: Workload, device="cpu") -> dict:
         "value": normal((S, Hkv, d), w.dtype, w.seed + 13, device),
         "key_cache": normal((w.num_blocks, Hkv, B, d), w.dtype, w.seed + 14, device),
         "value_cache": normal((w.num_blocks, Hkv, B, d), w.dtype, w.seed + 15, device),
+    }
+
+
+def prefill_tensors(w: Workload, device="cpu") -> dict:
+    """The random tensors of one prompt-phase step: the keys and values of the
+    cached prefix (the shared one, or with prefix_len 0 every sequence's
+    cached tokens back to back), and the queries, keys and values of every
+    request's own tokens (request-major, token-minor)."""
+    T = int(w.query_lens.sum())
+    Hkv, d = w.num_kv_heads, w.head_dim
+    # one shared prefix, or (prefix_len 0) each sequence's own cached tokens
+    P = w.prefix_len if w.prefix_len else int((w.context_lens - w.query_lens).sum())
+    return {
+        "prefix_key": normal((P, Hkv, d), w.dtype, w.seed + 31, device),
+        "prefix_value": normal((P, Hkv, d), w.dtype, w.seed + 32, device),
+        "query": normal((T, w.num_heads, d), w.dtype, w.seed + 33, device),
+        "key": normal((T, Hkv, d), w.dtype, w.seed + 34, device),
+        "value": normal((T, Hkv, d), w.dtype, w.seed + 35, device),
     }
 
 
