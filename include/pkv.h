@@ -190,7 +190,7 @@ pkv_status paged_attention_decode_noalloc(void *out_dev, const void *query_dev,
  *                       PKV_EINDEX (the call reads block 0 instead).
  * No workspace: the call allocates nothing.  num_seqs <= 65535; head_dim in
  * {64, 128}; block_size a power of two in [4, 128]; num_heads % num_kv_heads
- * == 0.  Asynchronous on `stream`; PKV_EINVAL for bad arguments, launching
+ * == 0; scale > 0 (usually 1/sqrt(head_dim)).  Asynchronous on `stream`; PKV_EINVAL for bad arguments, launching
  * nothing.
  * ------------------------------------------------------------------------- */
 pkv_status paged_attention_prefill(void *out_dev, const void *query_dev,

@@ -79,6 +79,18 @@ __device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t adesc, uint
         : "memory");
 }
 
+// Same with A read from TMEM (M rows in lanes, 16-bit elements packed two
+// per column, the lower half holding the even K index).
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // One thread: arrive once on `bar` when every MMA this thread issued so far
 // has completed (their shared-memory reads and TMEM writes are done).
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {

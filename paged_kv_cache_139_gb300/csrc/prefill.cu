@@ -12,25 +12,25 @@
 // plain prompt; with fewer new tokens the first tokens are a cached prefix.
 //
 // How (sm_103a):
-//   * One CTA per (128 new tokens, query head, sequence): the tokens' queries
-//     are the 128 rows (M) of both products.  The grid walks a sequence's
-//     tiles from the last (the most keys) to the first.
-//   * A producer warp loads the query tile (tiled TMA over the query tensor)
+//   * One CTA per (256 new tokens, query head, sequence): two query tiles of
+//     128 rows (M of both products) that take turns on the tensor core.  The
+//     grid walks a sequence's tiles from the last (the most keys) to the first.
+//   * A producer warp loads the query tiles (tiled TMA over the query tensor)
 //     and then, for each 128-key tile, the tile's K and V blocks (tiled TMA
 //     over the cache, one box of B tokens x 64 elements per block and
 //     64-element panel of d) into a two-stage ring.  Boxes land 128-byte
 //     swizzled, the layout the MMA descriptors describe.
 //   * One thread of the MMA warp issues tcgen05.mma: S = Q K^T (M 128, N 128,
-//     fp32 in TMEM) one tile ahead, then O += P V (N 64 per panel of d, V
-//     read MN-major straight from the cache layout), each group committed to
-//     an mbarrier.
-//   * Four softmax warps (one thread per row) read S from TMEM, mask keys
-//     after the row's position, keep a running max and sum in fp32 (log2
+//     fp32 in TMEM), then O += P V with P read from TMEM and V read MN-major
+//     straight from the cache layout (N 64 per panel of d).  While one tile's
+//     softmax runs, the tensor core computes the other tile's products.
+//   * Four softmax warps per tile (one thread per row) read S from TMEM, mask
+//     keys after the row's position, keep a running max and sum in fp32 (log2
 //     domain; the reference max moves only when it grows by more than 8, so
-//     probabilities stay below 2^8), write P as 16-bit to shared memory (for
-//     bf16 as a rounded part and its remainder) and rescale O in TMEM when a
-//     row's reference moved.  At the end they divide
-//     by the sum and store the rows.
+//     probabilities stay below 2^8), write P as 16-bit over the scores in
+//     TMEM (for bf16 as a rounded part and its remainder) and rescale O in
+//     TMEM when a row's reference moved.  At the end they divide by the sum
+//     and store the rows.
 //   * All waits are bounded; a wait that gives up latches a timeout, the CTA
 //     drains its copies and MMAs and frees its TMEM.
 #include <cfloat>
@@ -45,15 +45,17 @@
 namespace pkv {
 namespace {
 
-constexpr int kRows = 128;               // query rows per CTA
+constexpr int kRows = 128;               // query rows per tile (M of both products)
+constexpr int kTiles = 2;                // query tiles per CTA, alternating on the tensor core
 constexpr int kKeys = 128;               // keys per KV tile
 constexpr int kStages = 2;               // K/V ring depth
-constexpr int kSoftmaxWarps = 4;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kThreads = 6 * 32;
+constexpr int kSoftmaxWarps = 4;         // per query tile
+constexpr int kProducerWarp = kTiles * kSoftmaxWarps;
+constexpr int kMmaWarp = kProducerWarp + 1;
+constexpr int kThreads = (kMmaWarp + 1) * 32;
 constexpr uint32_t kPanelBytes = 128 * 128;   // 128 rows x 64 16-bit elements
-constexpr uint32_t kTmemCols = 256;           // S: 128 columns, O: up to 128
+constexpr uint32_t kTmemCols = 512;           // per tile: S/P 128 columns, O 128
+constexpr uint32_t kTileCols = 256;
 constexpr float kRescaleLog2 = 8.f;           // reference max moves past this growth
 
 struct PrefillArgs {
@@ -67,25 +69,29 @@ struct PrefillArgs {
     float scale_log2;                    // scale * log2(e)
 };
 
-// bf16 probabilities carry 8 significant bits: a row over a handful of keys
-// would see their rounding in its output.  For bf16 the kernel therefore
-// writes P = P_hi + P_lo (both bf16, P_lo the rounding remainder, together 16
-// significant bits) and accumulates both products; fp16 (11 bits) needs one.
-template <int D, bool SPLIT> struct PfLayout {
+// Shared memory: the two query tiles and the K/V ring.  P stays in TMEM,
+// over the tile's S columns.  The allocation is padded to keep one CTA per
+// SM (each CTA takes all 512 TMEM columns).
+template <int D> struct PfLayout {
     static constexpr int NP = D / 64;                              // panels of d
-    static constexpr int NPP = SPLIT ? 2 : 1;                       // P parts
-    static constexpr uint32_t q = 0;                                // NP panels
-    static constexpr uint32_t p = q + NP * kPanelBytes;             // NPP x 2 panels of keys
-    static constexpr uint32_t k = p + NPP * 2 * kPanelBytes;        // kStages x NP panels
+    static constexpr uint32_t q = 0;                                // kTiles x NP panels
+    static constexpr uint32_t k = q + kTiles * NP * kPanelBytes;    // kStages x NP panels
     static constexpr uint32_t v = k + kStages * NP * kPanelBytes;
     static constexpr uint32_t bars = v + kStages * NP * kPanelBytes;
     static constexpr uint32_t bytes = bars + 256;
-    static constexpr size_t alloc = bytes + 1024;                   // room to align the base
+    static constexpr size_t alloc = (bytes + 1024 > 120u * 1024u) ? bytes + 1024 : 120u * 1024u;
 };
 
 // barrier slots
-enum : int { bQFull = 0, bKFull = 1, bVFull = 3, bKEmpty = 5, bVEmpty = 7, bSFull = 9, bSFree = 10,
-             bPFull = 11, bODone = 12, bDrain = 13, kNumBars = 14 };
+enum : int { bQFull = 0, bKFull = 1, bVFull = 3, bKEmpty = 5, bVEmpty = 7, bSFull = 9, bPFull = 11, bODone = 13,
+             bDrain = 15, kNumBars = 16 };
+
+// 2^x by the hardware approximation (MUFU); 2^-inf = 0.
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 __device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity, long long limit) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, limit));
@@ -101,17 +107,30 @@ template <> __device__ __forceinline__ uint32_t pack16<__nv_bfloat16>(float x, f
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// Probabilities in TMEM.  Chunk c (keys 32c .. 32c+31) of the row is written
+// over its own score columns: 16 columns of packed 16-bit p (two keys per
+// column, the even key in the lower half) at 32c, and for bf16 16 columns of
+// the rounding remainder at 32c + 16.  The product's A operand for keys
+// 16t .. 16t+15 is then 8 columns at 32 (t / 2) + 8 (t % 2) (+ 16 for the
+// remainder).
+//
+// bf16 probabilities carry 8 significant bits: a row over a handful of keys
+// would see their rounding in its output, so for bf16 P = P_hi + P_lo (both
+// bf16, together 16 significant bits) and both products are accumulated;
+// fp16 (11 bits) needs one.
+__device__ __forceinline__ uint32_t p_col(int t, bool lo) { return 32 * (t >> 1) + 8 * (t & 1) + (lo ? 16 : 0); }
+
 template <int D, typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_prefill_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmq,
                          const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
-    using L = PfLayout<D, kBf16>;
+    using L = PfLayout<D>;
     constexpr int NP = L::NP;
     extern __shared__ uint8_t smem_pf[];
     uint8_t *sm = smem_pf + ((1024u - (smem_u32(smem_pf) & 1023u)) & 1023u);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int tile = (int)gridDim.x - 1 - (int)blockIdx.x;
+    const int pair = (int)gridDim.x - 1 - (int)blockIdx.x;
     const int h = blockIdx.y, s = blockIdx.z;
 
     pdl_wait();
@@ -120,16 +139,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q_begin = a.query_start[s], q_end = a.query_start[s + 1], ctx = a.context_lens[s];
     const int n = q_end - q_begin;
     const int B = 1 << a.log2_block;
-    const int t0 = tile * kRows;
+    const int t0 = pair * kTiles * kRows;
     if (n < 0 || q_begin < 0 || q_end > a.num_tokens || n > ctx || ctx > a.max_blocks * B) {
-        if (tid == 0 && tile == 0 && h == 0) latch(st, kFlagBadContext, s);
+        if (tid == 0 && pair == 0 && h == 0) latch(st, kFlagBadContext, s);
         return;
     }
     if (t0 >= n) return;                       // this sequence has fewer tiles
-    const int rows = min(kRows, n - t0);
-    const int pos0 = ctx - n + t0;             // position of row 0
-    const int pos_last = pos0 + rows - 1;
-    const int nkv = pos_last / kKeys + 1;      // key tiles this CTA reads
+    // per tile x: valid rows, position of row 0, key tiles read (tile 1 sees at least tile 0's keys)
+    const int rows0 = min(kRows, n - t0), rows1 = max(0, min(kRows, n - t0 - kRows));
+    const int pos00 = ctx - n + t0, pos01 = pos00 + kRows;
+    const int nkv0 = (pos00 + rows0 - 1) / kKeys + 1;
+    const int nkv1 = rows1 ? (pos01 + rows1 - 1) / kKeys + 1 : 0;
+    const int ntiles = rows1 ? 2 : 1;
+    const int nkv = max(nkv0, nkv1);
     const int g = h / a.group;
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::bars);
@@ -142,10 +164,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars[bKEmpty + i], 1);
             mbar_init(&bars[bVEmpty + i], 1);
         }
-        mbar_init(&bars[bSFull], 1);
-        mbar_init(&bars[bSFree], kSoftmaxWarps * 32);
-        mbar_init(&bars[bPFull], kSoftmaxWarps * 32);
-        mbar_init(&bars[bODone], 1);
+        for (int x = 0; x < kTiles; x++) {
+            mbar_init(&bars[bSFull + x], 1);
+            mbar_init(&bars[bPFull + x], kSoftmaxWarps * 32);
+            mbar_init(&bars[bODone + x], 1);
+        }
         mbar_init(&bars[bDrain], 1);
         fence_mbar_init();
     }
@@ -154,25 +177,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t tS = tmem, tO = tmem + kKeys;
 
     if (warp == kProducerWarp) {
-        // ---------------- producer: Q once, then K and V per key tile ----------------
+        // ---------------- producer: Q tiles once, then K and V per key tile ----------------
         const uint64_t pol_q = policy_evict_first();
         const uint64_t pol_kv = policy_evict_last();   // read again by the sequence's other tiles and heads
         bool ok = true;
         if (lane == 0) {
-            mbar_arrive_expect_tx(&bars[bQFull], NP * kPanelBytes);
-            for (int p = 0; p < NP; p++)
-                tma_load_3d(sm + L::q + p * kPanelBytes, &tmq, 64 * p, h, q_begin + t0, &bars[bQFull], pol_q);
+            mbar_arrive_expect_tx(&bars[bQFull], ntiles * NP * kPanelBytes);
+            for (int x = 0; x < ntiles; x++)
+                for (int p = 0; p < NP; p++)
+                    tma_load_3d(sm + L::q + (x * NP + p) * kPanelBytes, &tmq, 64 * p, h, q_begin + t0 + x * kRows,
+                                &bars[bQFull], pol_q);
         }
         const int32_t *row = a.block_tables + (size_t)s * a.max_blocks;
         const int nblk_used = (ctx + B - 1) >> a.log2_block;
-        const int bpt = kKeys >> a.log2_block;          // blocks per key tile (B <= 128)
+        const int bpt = kKeys >> a.log2_block;          // blocks per key tile: 1..32, one per lane
+        auto blocks_in = [&](int jj) { return min(bpt, nblk_used - jj * bpt); };
+        int cur = lane < blocks_in(0) ? row[lane] : 0;  // this lane's block of the current tile
         int j = 0;
         for (; j < nkv; j++) {
             const int stg = j & 1;
-            const int nb = min(bpt, nblk_used - j * bpt);
+            const int nb = blocks_in(j);
+            // the next tile's block id, read ahead of the waits
+            const int nxt = (j + 1 < nkv && lane < blocks_in(j + 1)) ? row[(j + 1) * bpt + lane] : 0;
+            int phys = cur;
+            if (lane < nb && (phys < 0 || phys >= a.num_blocks)) {
+                latch(st, kFlagBadBlock, phys);
+                phys = 0;                                   // keep the byte count; the output is flagged
+            }
             const uint32_t bytes = (uint32_t)nb * (uint32_t)B * 128u * NP;
             for (int which = 0; which < 2; which++) {       // K, then V
                 if (j >= kStages) {
@@ -183,23 +216,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive_expect_tx(full, bytes);
                 __syncwarp();
                 uint8_t *dst = sm + (which ? L::v : L::k) + (uint32_t)stg * NP * kPanelBytes;
-                for (int b = lane; b < nb; b += 32) {
-                    int phys = row[j * bpt + b];
-                    if (phys < 0 || phys >= a.num_blocks) {
-                        latch(st, kFlagBadBlock, phys);
-                        phys = 0;                           // keep the byte count; the output is flagged
-                    }
+                if (lane < nb)
                     for (int p = 0; p < NP; p++)
-                        tma_load_4d(dst + p * kPanelBytes + (uint32_t)b * B * 128u, which ? &tmv : &tmk, 64 * p, 0, g,
-                                    phys, full, pol_kv);
-                }
+                        tma_load_4d(dst + p * kPanelBytes + (uint32_t)lane * B * 128u, which ? &tmv : &tmk, 64 * p, 0,
+                                    g, phys, full, pol_kv);
             }
             if (!ok) break;
+            cur = nxt;
         }
         if (!ok) {
             if (lane == 0) latch(st, kFlagTimeout, j);
             // copies already issued must land before the CTA's memory is reused
-            for (int jj = max(0, j - kStages); jj <= min(j, nkv - 1); jj++) {
+            for (int jj = max(0, j - kStages); jj < j; jj++) {
                 mbar_wait(&bars[bKFull + (jj & 1)], (jj >> 1) & 1, kDrainLimitCycles);
                 mbar_wait(&bars[bVFull + (jj & 1)], (jj >> 1) & 1, kDrainLimitCycles);
             }
@@ -207,191 +235,218 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         // ---------------- MMA issue (one thread) ----------------
+        // Order: S_0(0) S_1(0), then per key tile j: O_0 += P_0 V_j, S_0(j+1), O_1 += P_1 V_j,
+        // S_1(j+1): while one tile's softmax runs, the tensor core works on the other's products.
+        // The products of one thread run in issue order, so S(j+1) overwrites P(j) only after
+        // O += P(j) V_j has read it.
         if (lane == 0) {
             const uint32_t id_s = tc::idesc_f16(kRows, kKeys, kBf16, false);
             const uint32_t id_o = tc::idesc_f16(kRows, 64, kBf16, true);
-            const uint32_t q_base = smem_u32(sm + L::q), p_base = smem_u32(sm + L::p);
-            auto issue_s = [&](int stg) {
+            const uint32_t q_base = smem_u32(sm + L::q);
+            auto issue_s = [&](int x, int stg) {
                 const uint32_t k_base = smem_u32(sm + L::k) + (uint32_t)stg * NP * kPanelBytes;
+                const uint32_t qx = q_base + (uint32_t)x * NP * kPanelBytes;
 #pragma unroll
                 for (int k = 0; k < D / 16; k++) {
                     const uint32_t off = (k / 4) * kPanelBytes + (k % 4) * 32;
-                    tc::mma_f16_ss(tS, tc::smem_desc_sw128(q_base + off, 1024, 1024),
+                    tc::mma_f16_ss(tmem + x * kTileCols, tc::smem_desc_sw128(qx + off, 1024, 1024),
                                    tc::smem_desc_sw128(k_base + off, 1024, 1024), id_s, k > 0);
                 }
+                tc::mma_commit(&bars[bSFull + x]);
             };
-            auto issue_o = [&](int stg, bool acc) {
+            auto issue_o = [&](int x, int stg, bool acc) {
                 const uint32_t v_base = smem_u32(sm + L::v) + (uint32_t)stg * NP * kPanelBytes;
+                const uint32_t tp = tmem + x * kTileCols, to = tp + kKeys;
 #pragma unroll
-                for (int part = 0; part < L::NPP; part++)
+                for (int part = 0; part < (kBf16 ? 2 : 1); part++)
 #pragma unroll
-                    for (int k = 0; k < kKeys / 16; k++) {
-                        const uint32_t aoff = part * 2 * kPanelBytes + (k / 4) * kPanelBytes + (k % 4) * 32;
+                    for (int t = 0; t < kKeys / 16; t++)
 #pragma unroll
                         for (int p = 0; p < NP; p++)
-                            tc::mma_f16_ss(tO + 64 * p, tc::smem_desc_sw128(p_base + aoff, 1024, 1024),
-                                           tc::smem_desc_sw128(v_base + p * kPanelBytes + k * 2048, 1024, 1024),
-                                           id_o, (acc || part > 0 || k > 0) ? 1u : 0u);
-                    }
+                            tc::mma_f16_ts(to + 64 * p, tp + p_col(t, part == 1),
+                                           tc::smem_desc_sw128(v_base + p * kPanelBytes + t * 2048, 1024, 1024),
+                                           id_o, (acc || part > 0 || t > 0) ? 1u : 0u);
             };
             bool ok = mbar_wait(&bars[bQFull], 0, kWaitLimitCycles) && mbar_wait(&bars[bKFull], 0, kWaitLimitCycles);
             int j = 0;
             if (ok) {
                 tc::fence_after();
-                issue_s(0);
+                for (int x = 0; x < ntiles; x++) issue_s(x, 0);
                 tc::mma_commit(&bars[bKEmpty]);
-                tc::mma_commit(&bars[bSFull]);
-                for (; j < nkv; j++) {
-                    if (j + 1 < nkv) {
-                        const int s1 = (j + 1) & 1;
-                        ok = mbar_wait(&bars[bKFull + s1], ((j + 1) >> 1) & 1, kWaitLimitCycles) &&
-                             mbar_wait(&bars[bSFree], j & 1, kWaitLimitCycles);
+                for (; j < nkv && ok; j++) {
+                    const int stg = j & 1;
+                    ok = mbar_wait(&bars[bVFull + stg], (j >> 1) & 1, kWaitLimitCycles);
+                    for (int x = 0; x < ntiles && ok; x++) {
+                        const int nkv_x = x ? nkv1 : nkv0;
+                        if (j >= nkv_x) continue;
+                        ok = mbar_wait(&bars[bPFull + x], j & 1, kWaitLimitCycles);
                         if (!ok) break;
                         tc::fence_after();
-                        issue_s(s1);
-                        tc::mma_commit(&bars[bKEmpty + s1]);
-                        tc::mma_commit(&bars[bSFull]);
+                        issue_o(x, stg, j > 0);
+                        if (j + 1 == nkv_x) {
+                            tc::mma_commit(&bars[bODone + x]);
+                        } else {
+                            ok = mbar_wait(&bars[bKFull + ((j + 1) & 1)], ((j + 1) >> 1) & 1, kWaitLimitCycles);
+                            if (!ok) break;
+                            tc::fence_after();
+                            issue_s(x, (j + 1) & 1);
+                        }
                     }
-                    ok = mbar_wait(&bars[bVFull + (j & 1)], (j >> 1) & 1, kWaitLimitCycles) &&
-                         mbar_wait(&bars[bPFull], j & 1, kWaitLimitCycles);
-                    if (!ok) break;
-                    tc::fence_after();
-                    issue_o(j & 1, j > 0);
-                    tc::mma_commit(&bars[bVEmpty + (j & 1)]);
-                    tc::mma_commit(&bars[bODone]);
+                    if (ok) {
+                        tc::mma_commit(&bars[bVEmpty + stg]);               // V_j read by every tile
+                        if (j + 1 < nkv) tc::mma_commit(&bars[bKEmpty + ((j + 1) & 1)]);   // K_{j+1} too
+                    }
                 }
             }
-            if (!ok) {
-                latch(st, kFlagTimeout, 1000000 + j);
-                // every MMA issued so far completes before TMEM is freed
-                tc::mma_commit(&bars[bDrain]);
-                mbar_wait(&bars[bDrain], 0, kDrainLimitCycles);
-            }
+            if (!ok) latch(st, kFlagTimeout, 1000000 + j);
+            // every MMA issued so far, and every arrive it makes, completes before the CTA
+            // frees its TMEM and shared memory
+            tc::mma_commit(&bars[bDrain]);
+            mbar_wait(&bars[bDrain], 0, ok ? kWaitLimitCycles : kDrainLimitCycles);
         }
         __syncwarp();
     } else {
-        // ---------------- softmax: one thread per query row ----------------
-        const int r = tid;                                   // 0..127, TMEM lane r
-        const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
-        const int my_pos = r < rows ? pos0 + r : pos_last;   // last key this row may see
-        float m_run = -INFINITY, l_run = 0.f;
+        // ---------------- softmax: one thread per query row of its tile ----------------
+        const int x = warp / kSoftmaxWarps;                  // query tile
+        const int r = tid % (kSoftmaxWarps * 32);            // row, TMEM lane
+        const uint32_t lane_off = (uint32_t)(32 * (warp % 4)) << 16;
+        const uint32_t tS = tmem + x * kTileCols + lane_off, tO = tS + kKeys;
         bool ok = true;
-        int j = 0;
-        for (; j < nkv; j++) {
-            ok = wait_warp(&bars[bSFull], j & 1, kWaitLimitCycles);
-            if (!ok) break;
-            tc::fence_after();
-            uint32_t sr[4][32];
-#pragma unroll
-            for (int c = 0; c < 4; c++) tc::tmem_ld32(tS + lane_off + 32 * c, sr[c]);
-#pragma unroll
-            for (int c = 0; c < 4; c++) tc::tmem_wait_ld(sr[c]);
-            tc::fence_before();
-            mbar_arrive(&bars[bSFree]);                      // S may be overwritten by the next tile
-
-            const int lim = my_pos - j * kKeys;              // keys 0..lim of this tile are visible
-            float mx = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < 4; c++)
-#pragma unroll
-                for (int i = 0; i < 32; i++) {
-                    float x = __uint_as_float(sr[c][i]) * a.scale_log2;
-                    x = (32 * c + i <= lim) ? x : -INFINITY;
-                    sr[c][i] = __float_as_uint(x);
-                    mx = fmaxf(mx, x);
-                }
-            const bool moved = mx > m_run + kRescaleLog2;
-            const float m_new = moved ? mx : m_run;
-            const float alpha = exp2f(m_run - m_new);        // 0 on the first tile, 1 when not moved
-            m_run = m_new;
-            float lsum = 0.f;
-#pragma unroll
-            for (int c = 0; c < 4; c++)
-#pragma unroll
-                for (int i = 0; i < 32; i++) {
-                    const float pv = exp2f(__uint_as_float(sr[c][i]) - m_run);
-                    lsum += pv;
-                    sr[c][i] = __float_as_uint(pv);              // the score register now holds p
-                }
-            l_run = l_run * alpha + lsum;
-
-            if (j > 0) {                                     // PV of the previous tile: O stable, P free
-                ok = wait_warp(&bars[bODone], (j - 1) & 1, kWaitLimitCycles);
+        const int rows_x = x ? rows1 : rows0, pos0_x = x ? pos01 : pos00, nkv_x = x ? nkv1 : nkv0;
+        if (rows_x > 0) {
+            const int my_pos = r < rows_x ? pos0_x + r : pos0_x + rows_x - 1;   // last key this row sees
+            float m_run = -INFINITY, l_run = 0.f;
+            // the tile that zeroes V rows past the context (before its product reads them)
+            const bool zero_duty = (x == 0) == (nkv0 == nkv);
+            int j = 0;
+            for (; j < nkv_x; j++) {
+                ok = wait_warp(&bars[bSFull + x], j & 1, kWaitLimitCycles);
                 if (!ok) break;
                 tc::fence_after();
-                if (__any_sync(0xffffffffu, moved)) {
+                const int lim = my_pos - j * kKeys;          // keys 0..lim of this tile are visible
+                // Tiles below the diagonal are visible to every row of the warp: no mask, and the
+                // scale folds into the exponent (the scale is positive, so the raw maximum is the
+                // scaled one's).
+                const bool full = __all_sync(0xffffffffu, lim >= kKeys - 1);
+                const float c2 = a.scale_log2;
+                // pass 1, the row maximum: the row's 128 scores in four loads, one wait
+                float mxs[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                {
+                    uint32_t sr[4][32];
+#pragma unroll
+                    for (int c = 0; c < 4; c++) tc::tmem_ld32(tS + 32 * c, sr[c]);
+#pragma unroll
+                    for (int c = 0; c < 4; c++) tc::tmem_wait_ld(sr[c]);
+                    if (full) {
+#pragma unroll
+                        for (int c = 0; c < 4; c++)
+#pragma unroll
+                            for (int i = 0; i < 32; i++) mxs[i & 3] = fmaxf(mxs[i & 3], __uint_as_float(sr[c][i]));
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 4; c++)
+#pragma unroll
+                            for (int i = 0; i < 32; i++)
+                                if (32 * c + i <= lim) mxs[i & 3] = fmaxf(mxs[i & 3], __uint_as_float(sr[c][i]));
+                    }
+                }
+                const float mraw = fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3]));
+                const float mx = mraw * c2;                   // -inf when no key of the tile is visible
+                const bool moved = mx > m_run + kRescaleLog2;
+                const float m_new = moved ? mx : m_run;
+                const float alpha = fast_exp2(m_run - m_new);  // 0 on the first tile, 1 when not moved
+                m_run = m_new;
+                // O of the previous tiles is complete (its products were issued before this S)
+                if (j > 0 && __any_sync(0xffffffffu, moved)) {
 #pragma unroll
                     for (int c = 0; c < D / 32; c++) {
                         uint32_t o[32];
-                        tc::tmem_ld32(tO + lane_off + 32 * c, o);
+                        tc::tmem_ld32(tO + 32 * c, o);
                         tc::tmem_wait_ld(o);
 #pragma unroll
                         for (int i = 0; i < 32; i++) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tc::tmem_st32(tO + lane_off + 32 * c, o);
-                    }
-                    tc::tmem_wait_st();
-                }
-            }
-            const int kbase = j * kKeys;
-            if (j == nkv - 1 && kbase + kKeys > ctx) {
-                // rows past the end of the context hold other data: P is 0 there, but 0 x NaN is not
-                ok = wait_warp(&bars[bVFull + (j & 1)], (j >> 1) & 1, kWaitLimitCycles);
-                if (!ok) break;
-                const int first = ctx - kbase;
-                uint8_t *vs = sm + L::v + (uint32_t)(j & 1) * NP * kPanelBytes;
-                const int nvec = (kKeys - first) * 8;        // 16-byte vectors per panel
-                for (int i = tid; i < nvec * NP; i += kSoftmaxWarps * 32) {
-                    const int p = i / nvec, rem = i % nvec;
-                    *reinterpret_cast<uint4 *>(vs + p * kPanelBytes + (first + rem / 8) * 128 + (rem % 8) * 16) =
-                        make_uint4(0u, 0u, 0u, 0u);
-                }
-            }
-            uint8_t *ps = sm + L::p;
-#pragma unroll
-            for (int q = 0; q < 16; q++) {
-                const int panel = q >> 3, c = q & 7;
-                const uint32_t *pv = &sr[q / 4][8 * (q % 4)];
-                uint32_t hi[4], lo[4];
-#pragma unroll
-                for (int e = 0; e < 4; e++) {
-                    const float p0 = __uint_as_float(pv[2 * e]), p1 = __uint_as_float(pv[2 * e + 1]);
-                    hi[e] = pack16<T>(p0, p1);
-                    if (kBf16)   // remainder after rounding (bf16 widens exactly by a shift)
-                        lo[e] = pack16<T>(p0 - __uint_as_float(hi[e] << 16), p1 - __uint_as_float(hi[e] & 0xffff0000u));
-                }
-                const uint32_t off = panel * kPanelBytes + r * 128 + ((c ^ (r & 7)) << 4);
-                *reinterpret_cast<uint4 *>(ps + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                if (kBf16)
-                    *reinterpret_cast<uint4 *>(ps + 2 * kPanelBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-            }
-            fence_proxy_async_smem();                        // generic writes -> tensor-core reads
-            tc::fence_before();
-            mbar_arrive(&bars[bPFull]);
-        }
-        if (ok) ok = wait_warp(&bars[bODone], (nkv - 1) & 1, kWaitLimitCycles);
-        if (ok) {
-            tc::fence_after();
-            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-            T *orow = reinterpret_cast<T *>(a.out) + ((size_t)(q_begin + t0 + r) * a.num_heads + h) * D;
-#pragma unroll
-            for (int c = 0; c < D / 32; c++) {
-                uint32_t o[32];
-                tc::tmem_ld32(tO + lane_off + 32 * c, o);
-                tc::tmem_wait_ld(o);
-                if (r < rows) {
-#pragma unroll
-                    for (int v = 0; v < 4; v++) {
-                        uint4 w;
-                        w.x = pack16<T>(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
-                        w.y = pack16<T>(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
-                        w.z = pack16<T>(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
-                        w.w = pack16<T>(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-                        *reinterpret_cast<uint4 *>(orow + 32 * c + 8 * v) = w;
+                        tc::tmem_st32(tO + 32 * c, o);
                     }
                 }
+                const int kbase = j * kKeys;
+                if (zero_duty && j == nkv - 1 && kbase + kKeys > ctx) {
+                    // rows past the end of the context hold other data: P is 0 there, but 0 x NaN is not
+                    ok = wait_warp(&bars[bVFull + (j & 1)], (j >> 1) & 1, kWaitLimitCycles);
+                    if (!ok) break;
+                    const int first = ctx - kbase;
+                    uint8_t *vs = sm + L::v + (uint32_t)(j & 1) * NP * kPanelBytes;
+                    const int nvec = (kKeys - first) * 8;    // 16-byte vectors per panel
+                    for (int i = r; i < nvec * NP; i += kSoftmaxWarps * 32) {
+                        const int p = i / nvec, rem = i % nvec;
+                        *reinterpret_cast<uint4 *>(vs + p * kPanelBytes + (first + rem / 8) * 128 + (rem % 8) * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    fence_proxy_async_smem();                // generic writes -> tensor-core reads
+                }
+                // pass 2, probabilities written over the scores: two halves, two loads each
+                const float neg_m = -m_run;
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int hf = 0; hf < 2; hf++) {
+                    uint32_t sr[2][32];
+#pragma unroll
+                    for (int c = 0; c < 2; c++) tc::tmem_ld32(tS + 64 * hf + 32 * c, sr[c]);
+#pragma unroll
+                    for (int c = 0; c < 2; c++) tc::tmem_wait_ld(sr[c]);
+#pragma unroll
+                    for (int c = 0; c < 2; c++) {
+                        const int kc = 32 * (2 * hf + c);
+                        uint32_t pk[32];
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            float p0 = fast_exp2(fmaf(__uint_as_float(sr[c][i]), c2, neg_m));
+                            float p1 = fast_exp2(fmaf(__uint_as_float(sr[c][i + 1]), c2, neg_m));
+                            if (!full) {
+                                p0 = kc + i <= lim ? p0 : 0.f;
+                                p1 = kc + i + 1 <= lim ? p1 : 0.f;
+                            }
+                            ls[(i >> 1) & 3] += p0 + p1;
+                            const uint32_t hi = pack16<T>(p0, p1);
+                            pk[i / 2] = hi;
+                            // remainder after rounding (bf16 widens exactly by a shift)
+                            pk[16 + i / 2] = kBf16 ? pack16<T>(p0 - __uint_as_float(hi << 16),
+                                                               p1 - __uint_as_float(hi & 0xffff0000u))
+                                                   : 0u;
+                        }
+                        tc::tmem_st32(tS + 64 * hf + 32 * c, pk);
+                    }
+                }
+                l_run = l_run * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+                tc::tmem_wait_st();
+                tc::fence_before();
+                mbar_arrive(&bars[bPFull + x]);
             }
-        } else if (lane == 0) {
-            latch(st, kFlagTimeout, 2000000 + j);
+            if (ok) ok = wait_warp(&bars[bODone + x], 0, kWaitLimitCycles);
+            if (ok) {
+                tc::fence_after();
+                const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+                T *orow = reinterpret_cast<T *>(a.out) +
+                          ((size_t)(q_begin + t0 + x * kRows + r) * a.num_heads + h) * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; c++) {
+                    uint32_t o[32];
+                    tc::tmem_ld32(tO + 32 * c, o);
+                    tc::tmem_wait_ld(o);
+                    if (r < rows_x) {
+#pragma unroll
+                        for (int v = 0; v < 4; v++) {
+                            uint4 w;
+                            w.x = pack16<T>(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
+                            w.y = pack16<T>(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
+                            w.z = pack16<T>(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
+                            w.w = pack16<T>(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
+                            *reinterpret_cast<uint4 *>(orow + 32 * c + 8 * v) = w;
+                        }
+                    }
+                }
+            } else if (lane == 0) {
+                latch(st, kFlagTimeout, 2000000 + j);
+            }
         }
     }
     tc::fence_before();
@@ -406,7 +461,7 @@ template <int D, typename T>
 cudaError_t launch_prefill(const PrefillArgs &a, const void *query, const void *kc, const void *vc, int Hkv,
                            int max_query_len, cudaStream_t stream) {
     constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
-    using L = PfLayout<D, kBf16>;
+    using L = PfLayout<D>;
     auto kern = paged_prefill_kernel<D, T>;
     static bool configured = false;
     if (!configured) {
@@ -430,7 +485,9 @@ cudaError_t launch_prefill(const PrefillArgs &a, const void *query, const void *
     if (!encode_tiled16(&tmq, query, 3, qdims, qstr, qbox, kBf16) || !encode_tiled16(&tmk, kc, 4, cdims, cstr, cbox, kBf16) ||
         !encode_tiled16(&tmv, vc, 4, cdims, cstr, cbox, kBf16))
         return cudaErrorInvalidValue;
-    const dim3 grid((unsigned)((max_query_len + kRows - 1) / kRows), (unsigned)a.num_heads, (unsigned)a.num_seqs);
+    const int rows_per_cta = kTiles * kRows;
+    const dim3 grid((unsigned)((max_query_len + rows_per_cta - 1) / rows_per_cta), (unsigned)a.num_heads,
+                    (unsigned)a.num_seqs);
     return launch(kern, grid, dim3(kThreads), L::alloc, stream, a, tmq, tmk, tmv);
 }
 
@@ -458,8 +515,8 @@ extern "C" pkv_status paged_attention_prefill(void *out, const void *query, cons
     if (!is_pow2(block_size) || block_size < 4 || block_size > 128)
         return fail(PKV_EINVAL, "paged_attention_prefill: block_size %d not a power of two in [4, 128]", block_size);
     if (dtype != PKV_F16 && dtype != PKV_BF16) return fail(PKV_EINVAL, "paged_attention_prefill: bad dtype %d", (int)dtype);
-    if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
-        return fail(PKV_EINVAL, "paged_attention_prefill: scale not finite");
+    if (!(scale > 0.f) || scale == INFINITY)
+        return fail(PKV_EINVAL, "paged_attention_prefill: scale must be positive and finite");
     if (num_seqs == 0 || num_tokens == 0) return PKV_OK;
     if (max_query_len == 0 || max_query_len > num_tokens) max_query_len = num_tokens;
     if (num_blocks <= 0 || max_blocks_per_seq <= 0)

@@ -77,7 +77,7 @@ def _call_prefill(**over):
 @pytest.mark.parametrize("over", [
     dict(d=96), dict(d=0), dict(B=12), dict(B=2), dict(B=256), dict(H=5, Hkv=2), dict(Hkv=0), dict(dt=7),
     dict(S=-1), dict(T=-3), dict(mql=-1), dict(S=70000), dict(out=None), dict(qs=None), dict(query=18),
-    dict(NB=0), dict(scale=float("inf")), dict(scale=float("nan")),
+    dict(NB=0), dict(scale=float("inf")), dict(scale=float("nan")), dict(scale=0.0), dict(scale=-0.1),
 ])
 def test_prefill_rejects_bad_arguments(over):
     assert _call_prefill(**over) == 1                    # PKV_EINVAL, before any launch
