@@ -22,7 +22,7 @@
 //     swizzled, the layout the MMA descriptors describe.
 //   * One thread of the MMA warp issues tcgen05.mma: S = Q K^T (M 128, N 128,
 //     fp32 in TMEM), then O += P V with P read from TMEM and V read MN-major
-//     straight from the cache layout (N 64 per panel of d).  While one tile's
+//     straight from the cache layout (N = d: one product per 16 keys).  While one tile's
 //     softmax runs, the tensor core computes the other tile's products.
 //   * Four softmax warps per tile (one thread per row) read S from TMEM, mask
 //     keys after the row's position, keep a running max and sum in fp32 (log2
@@ -241,7 +241,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // O += P(j) V_j has read it.
         if (lane == 0) {
             const uint32_t id_s = tc::idesc_f16(kRows, kKeys, kBf16, false);
-            const uint32_t id_o = tc::idesc_f16(kRows, 64, kBf16, true);
+            // O += P V: one product of N = D per 16 keys (for D = 128 the two 64-wide panels of V
+            // are 16 KB apart, the descriptor's leading byte offset)
+            const uint32_t id_o = tc::idesc_f16(kRows, D, kBf16, true);
             const uint32_t q_base = smem_u32(sm + L::q);
             auto issue_s = [&](int x, int stg) {
                 const uint32_t k_base = smem_u32(sm + L::k) + (uint32_t)stg * NP * kPanelBytes;
@@ -261,11 +263,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int part = 0; part < (kBf16 ? 2 : 1); part++)
 #pragma unroll
                     for (int t = 0; t < kKeys / 16; t++)
-#pragma unroll
-                        for (int p = 0; p < NP; p++)
-                            tc::mma_f16_ts(to + 64 * p, tp + p_col(t, part == 1),
-                                           tc::smem_desc_sw128(v_base + p * kPanelBytes + t * 2048, 1024, 1024),
-                                           id_o, (acc || part > 0 || t > 0) ? 1u : 0u);
+                        tc::mma_f16_ts(to, tp + p_col(t, part == 1),
+                                       tc::smem_desc_sw128(v_base + t * 2048, kPanelBytes, 1024), id_o,
+                                       (acc || part > 0 || t > 0) ? 1u : 0u);
             };
             bool ok = mbar_wait(&bars[bQFull], 0, kWaitLimitCycles) && mbar_wait(&bars[bKFull], 0, kWaitLimitCycles);
             int j = 0;
