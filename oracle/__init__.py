@@ -10,7 +10,8 @@ Contents:
                  token per sequence; prompt phase: many, causal), the
                  slot-mapped cache write, the block copy, per-partition statistics and their
                  log-sum-exp merge (built by build.py with gcc).
-  allocator.py   the reference ref-counted block allocator.
+  allocator.py   the reference ref-counted block allocator (with the move of
+                 a sequence group to a second pool, for swapping).
 
 Parity status: every function here is pinned by tests/test_oracle_pins.py
 and tests/test_oracle_allocator.py (worked examples from the pages, closed
@@ -28,7 +29,7 @@ from .allocator import AllocatorOOM, RefAllocator, blocks_needed
 from .build import LIB, build
 
 __all__ = ["AllocatorOOM", "RefAllocator", "blocks_needed", "kv_bytes_per_token",
-           "cache_write", "copy_blocks", "paged_attention", "partition_stats",
+           "cache_write", "copy_blocks", "copy_blocks_between", "paged_attention", "partition_stats",
            "merge_partitions", "paged_prefill", "locate_tokens", "decode16", "bits16", "lib"]
 
 _lib = None
@@ -47,6 +48,7 @@ def load(path) -> ctypes.CDLL:
     L.oracle_locate_tokens.argtypes = [_p, _i, _i64, _p, _p]
     L.oracle_cache_write.argtypes = [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i]
     L.oracle_copy_blocks.argtypes = [_p, _p, _i, _i64, _i]
+    L.oracle_copy_blocks_between.argtypes = [_p, _p, _p, _i, _i64, _i, _i]
     L.oracle_paged_attention.argtypes = [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i,
                                          _d, _i, _i, _p, _i]
     L.oracle_paged_prefill.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i,
@@ -140,6 +142,17 @@ def copy_blocks(cache: np.ndarray, pairs) -> None:
     assert cache.flags.c_contiguous
     _check(lib().oracle_copy_blocks(_ptr(cache), _ptr(pr), pr.shape[0],
                                     int(np.prod(cache.shape[1:])), NB), "copy_blocks")
+
+
+def copy_blocks_between(dst_pool: np.ndarray, src_pool: np.ndarray, pairs) -> None:
+    """In place on the uint16 array dst_pool [NBd][...]: block pairs[i][1] of
+    dst_pool takes block pairs[i][0] of src_pool."""
+    pr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
+    assert dst_pool.flags.c_contiguous and src_pool.flags.c_contiguous
+    assert dst_pool.shape[1:] == src_pool.shape[1:]
+    _check(lib().oracle_copy_blocks_between(_ptr(dst_pool), _ptr(np.ascontiguousarray(src_pool)), _ptr(pr),
+                                            pr.shape[0], int(np.prod(dst_pool.shape[1:])), src_pool.shape[0],
+                                            dst_pool.shape[0]), "copy_blocks_between")
 
 
 def default_scale(head_dim: int) -> float:

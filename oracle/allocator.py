@@ -20,6 +20,12 @@ Rules and their sources:
     reaches zero returns to the pool ("vLLM & PagedAttention" §VII, Fig. 9).
   * fork, append and free are the three sequence primitives ("vLLM &
     PagedAttention" §X).
+  * Swapping ("vLLM & PagedAttention" §VIII and Fig. 4): the blocks of an
+    evicted sequence group move to a second (CPU) allocator and back.  A
+    group leaves all together or not at all; sequences that share blocks go
+    together, so a group must hold every reference to its blocks.  Sharing
+    survives the move: each distinct block gets one block in the other pool,
+    with the same reference count.
 
 Where the pages are silent (which free block is handed out next), this reads:
 the pool hands blocks out in a given initial order; freed blocks are pushed
@@ -123,6 +129,45 @@ class RefAllocator:
             self.ref[b] -= 1
             if self.ref[b] == 0:
                 self._free.append(b)
+
+    # -- swapping between pools ---------------------------------------------
+    def move_group(self, dst: "RefAllocator", seqs):
+        """Move the sequences `seqs` (a group holding every reference to its
+        blocks) into `dst`, all or nothing.  Returns (new ids in dst, pairs)
+        where pairs lists (block here, block in dst) for every distinct block,
+        in first-seen order; the device copies these pairs."""
+        seqs = [int(s) for s in seqs]
+        if dst.B != self.B:
+            raise ValueError("pools of different block sizes")
+        if len(set(seqs)) != len(seqs) or any(s not in self._seqs for s in seqs):
+            raise ValueError("unknown or repeated sequence")
+        uses: dict[int, int] = {}
+        order: list[int] = []
+        for s in seqs:
+            for b in self._seqs[s]["blocks"]:
+                if b not in uses:
+                    uses[b] = 0
+                    order.append(b)
+                uses[b] += 1
+        if any(self.ref[b] != n for b, n in uses.items()):
+            raise ValueError("the group shares blocks with a sequence outside it")
+        if len(order) > dst.num_free():
+            raise AllocatorOOM(f"need {len(order)} blocks in the other pool, {dst.num_free()} free")
+        remap = {}
+        for b in order:
+            c = dst._pop()
+            dst.ref[c] = uses[b]
+            remap[b] = c
+        new_ids = []
+        for s in seqs:
+            st = self._seqs[s]
+            sid = dst._next_id
+            dst._next_id += 1
+            dst._seqs[sid] = {"blocks": [remap[b] for b in st["blocks"]], "len": st["len"]}
+            new_ids.append(sid)
+        for s in seqs:
+            self.free(s)
+        return new_ids, [(b, remap[b]) for b in order]
 
     # -- batched step ------------------------------------------------------
     def append_batch(self, seqs):

@@ -18,6 +18,8 @@
  *   - "vLLM & PagedAttention" §X: fused reshape + block write (new K/V written
  *     at block-table positions) and fused block copy (copy-on-write copies of
  *     scattered blocks).
+ *   - same page, §VIII: swapping copies an evicted group's blocks to a CPU
+ *     pool and back (block copies between two pools).
  *
  * Layouts (the pages leave the "read-optimized layout" open; this is the
  * reading the whole build uses):
@@ -143,6 +145,24 @@ int oracle_copy_blocks(uint16_t *cache, const int32_t *pairs, int n,
             return -2;
         for (int64_t i = 0; i < block_elems; i++)
             cache[(int64_t)dst * block_elems + i] = cache[(int64_t)src * block_elems + i];
+    }
+    return 0;
+}
+
+/* Copies between two pools (swapping, "vLLM & PagedAttention" §VIII): for
+ * each pair, block dst_pool[pairs[i][1]] := src_pool[pairs[i][0]]; every
+ * other block of dst_pool is untouched. */
+int oracle_copy_blocks_between(uint16_t *dst_pool, const uint16_t *src_pool, const int32_t *pairs, int n,
+                               int64_t block_elems, int src_blocks, int dst_blocks)
+{
+    if (n < 0 || block_elems <= 0)
+        return -1;
+    for (int p = 0; p < n; p++) {
+        int32_t src = pairs[2 * p], dst = pairs[2 * p + 1];
+        if (src < 0 || src >= src_blocks || dst < 0 || dst >= dst_blocks)
+            return -2;
+        for (int64_t i = 0; i < block_elems; i++)
+            dst_pool[(int64_t)dst * block_elems + i] = src_pool[(int64_t)src * block_elems + i];
     }
     return 0;
 }

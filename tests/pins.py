@@ -465,6 +465,142 @@ def pin_prefill_which_subset():
     assert np.isnan(part[1, 1]).all()
 
 
+# -- swapping between a GPU and a CPU pool ------------------------------------------
+
+def _alloc_state(a):
+    return (list(a.ref), a.free_list(), {k: (list(v["blocks"]), v["len"]) for k, v in a._seqs.items()})
+
+
+def _sampling_group(a, prompt=10, samples=3, suffix=(2, 0, 5)):
+    """A prompt forked into samples that each append a suffix (copy on write
+    of the shared, partly filled last block)."""
+    root = a.seq_new(prompt)
+    ids = [root] + [a.fork(root) for _ in range(samples - 1)]
+    for sid, n in zip(ids, suffix):
+        for _ in range(n):
+            a.append(sid)
+    return ids
+
+
+def pin_swap_all_or_nothing():
+    """A group that does not fit in the other pool moves not at all."""
+    g = oracle.RefAllocator(16, 4)
+    ids = _sampling_group(g)
+    need = len({b for s in ids for b in g.block_table(s)})
+    c = oracle.RefAllocator(need - 1, 4)
+    before_g, before_c = _alloc_state(g), _alloc_state(c)
+    try:
+        g.move_group(c, ids)
+        raise AssertionError("a group larger than the free pool moved")
+    except oracle.AllocatorOOM:
+        pass
+    assert _alloc_state(g) == before_g and _alloc_state(c) == before_c
+
+
+def pin_swap_preserves_sharing():
+    """Moving out and back keeps lengths, the sharing pattern and the
+    reference counts; the source pool gets every block back."""
+    g = oracle.RefAllocator(32, 4, free_order=np.random.default_rng(5).permutation(32))
+    ids = _sampling_group(g, prompt=13, samples=4, suffix=(3, 0, 1, 6))
+    tables = [g.block_table(s) for s in ids]
+    lens = [g.seq_len(s) for s in ids]
+    refs = {b: g.block_ref(b) for t in tables for b in t}
+    free0 = g.num_free() + len(refs)
+    c = oracle.RefAllocator(24, 4)
+    cids, pairs = g.move_group(c, ids)
+    assert g.num_free() == free0 and len(pairs) == len(refs)
+    remap = dict(pairs)
+    assert [c.block_table(s) for s in cids] == [[remap[b] for b in t] for t in tables]
+    assert all(c.block_ref(remap[b]) == n for b, n in refs.items())
+    assert [c.seq_len(s) for s in cids] == lens
+    gids, back = c.move_group(g, cids)
+    assert c.num_free() == 24
+    # the same structure again (block ids may differ)
+    t2 = [g.block_table(s) for s in gids]
+    eq = lambda ts: [[ts[i][x] == ts[j][y] for j in range(len(ts)) for y in range(len(ts[j]))]
+                     for i in range(len(ts)) for x in range(len(ts[i]))]
+    assert eq(t2) == eq(tables) and [g.seq_len(s) for s in gids] == lens
+
+
+def pin_swap_group_must_hold_all_references():
+    """Sequences sharing blocks are evicted together: half a group is refused."""
+    g = oracle.RefAllocator(16, 4)
+    ids = _sampling_group(g)
+    c = oracle.RefAllocator(16, 4)
+    before = _alloc_state(g)
+    try:
+        g.move_group(c, ids[:1])
+        raise AssertionError("half of a sharing group moved")
+    except ValueError:
+        pass
+    assert _alloc_state(g) == before
+
+
+def pin_swap_space_bound():
+    """A CPU pool as large as the GPU pool always holds everything swapped out
+    (one can never swap out more than exists)."""
+    rng = np.random.default_rng(9)
+    g = oracle.RefAllocator(40, 4, free_order=rng.permutation(40))
+    groups = []
+    while True:
+        try:
+            groups.append(_sampling_group(g, prompt=int(rng.integers(1, 9)), samples=2,
+                                          suffix=(int(rng.integers(0, 4)), int(rng.integers(0, 4)))))
+        except oracle.AllocatorOOM:
+            break
+    c = oracle.RefAllocator(40, 4)
+    for grp in groups:
+        g.move_group(c, grp)
+    rest = list(g._seqs)                 # what the last, failed group had created
+    if rest:
+        g.move_group(c, rest)
+    assert g.num_free() == 40 and c.num_free() == 40 - sum(1 for b in range(40) if c.block_ref(b))
+
+
+def pin_copy_between_exact():
+    """Only the destination blocks of the pairs change, each to its source."""
+    rng = np.random.default_rng(13)
+    src = rng.integers(0, 65536, size=(7, 2, 4, 8), dtype=np.uint16)
+    dst = rng.integers(0, 65536, size=(5, 2, 4, 8), dtype=np.uint16)
+    pairs = [(6, 0), (2, 3), (6, 4)]
+    want = dst.copy()
+    for s_, d_ in pairs:
+        want[d_] = src[s_]
+    oracle.copy_blocks_between(dst, src, pairs)
+    assert np.array_equal(dst, want)
+
+
+def pin_swap_round_trip_attention():
+    """Swapping a group out (device copy to the CPU pool), clobbering the GPU
+    pool and swapping it back in leaves every sequence's attention output
+    bit-identical."""
+    H, d, B = 2, 8, 4
+    g = oracle.RefAllocator(24, B, free_order=np.random.default_rng(3).permutation(24))
+    ids = _sampling_group(g, prompt=9, samples=3, suffix=(4, 1, 0))
+    kg = _pool(24, H, B, d, torch.float16, 141)
+    vg = _pool(24, H, B, d, torch.float16, 142)
+    q = _rand16((3, H, d), torch.float16, 143)
+    def attend(a, sids, kc, vc):
+        bt = np.full((3, 8), -1, np.int32)
+        for i, s_ in enumerate(sids):
+            t = a.block_table(s_)
+            bt[i, :len(t)] = t
+        return oracle.paged_attention(q, kc, vc, bt, np.array([a.seq_len(s_) for s_ in sids]), "f16")
+    before = attend(g, ids, kg, vg)
+    c = oracle.RefAllocator(16, B)
+    kc = np.zeros((16, H, B, d), np.uint16)
+    vc = np.zeros((16, H, B, d), np.uint16)
+    cids, out_pairs = g.move_group(c, ids)
+    oracle.copy_blocks_between(kc, kg, out_pairs)
+    oracle.copy_blocks_between(vc, vg, out_pairs)
+    kg[:] = 0x7E00                                   # NaN everywhere on the GPU side
+    vg[:] = 0x7E00
+    gids, in_pairs = c.move_group(g, cids)
+    oracle.copy_blocks_between(kg, kc, in_pairs)
+    oracle.copy_blocks_between(vg, vc, in_pairs)
+    assert np.array_equal(attend(g, gids, kg, vg), before)
+
+
 def pin_kv_size():
     g = golden("kv_size_opt13b.json")
     per = oracle.kv_bytes_per_token(g["hidden"], g["layers"], g["bytes_per_number"])

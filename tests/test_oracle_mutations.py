@@ -42,6 +42,10 @@ MUTANTS = [
     ("prefill gqa map modulo", "h / (H / Hkv), d, scale, is_bf16, &m, &l, o, x);",
      "h % Hkv, d, scale, is_bf16, &m, &l, o, x);", 0),
     ("prefill no normalisation", "o[i] = l > 0.0 ? o[i] / l : 0.0;", "o[i] = l > 0.0 ? o[i] : 0.0;", 1),
+    ("copy between pools reversed", "dst_pool[(int64_t)dst * block_elems + i] = src_pool[(int64_t)src * block_elems + i];",
+     "dst_pool[(int64_t)src * block_elems + i] = src_pool[(int64_t)dst * block_elems + i];", 0),
+    ("copy between pools skips the last pair", "for (int p = 0; p < n; p++) {\n        int32_t src = pairs[2 * p], dst",
+     "for (int p = 0; p + 1 < n; p++) {\n        int32_t src = pairs[2 * p], dst", 0),
     ("max not tracked", "if (x[t - t0] > m)\n            m = x[t - t0];", "if (x[t - t0] > m)\n            m = 0.0;", 0),
 ]
 
