@@ -41,6 +41,7 @@ import workloads  # noqa: E402
 
 METRIC = "paged decode attention effective KV-read GB/s and % of GB300 HBM peak"
 PREFILL_METRIC = "prompt-phase paged attention TFLOP/s (causal, after a shared prefix)"
+SWAP_METRIC = "swap GB/s (KV blocks GPU -> pinned host -> GPU, both directions)"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 512 << 20
@@ -53,7 +54,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="opt13b",
-                    choices=["tiny", "opt13b", "llama7b", "sampling", "longgqa", "prefix"])
+                    choices=["tiny", "opt13b", "llama7b", "sampling", "longgqa", "prefix", "swap"])
     ap.add_argument("--block-size", type=int, default=16)
     ap.add_argument("--head-dim", type=int, default=128, choices=[64, 128])
     ap.add_argument("--partition-size", type=int, default=-1)
@@ -67,6 +68,8 @@ def make_workload(args, rank: int) -> workloads.Workload:
     if args.workload == "llama7b":
         kw["block_size"] = args.block_size
         kw["head_dim"] = args.head_dim
+    if args.workload == "swap":
+        kw["block_size"] = args.block_size
     w = workloads.by_name(args.workload, **kw)
     if rank:
         w = workloads.by_name(args.workload, seed=w.seed + 7919 * rank, **kw) if args.workload != "tiny" else w
@@ -202,6 +205,8 @@ def run_reference(args, rank: int, world: int):
     w = make_workload(args, 0)
     if w.query_lens is not None:
         return run_reference_prefill(args, w)
+    if args.workload == "swap":
+        return run_reference_swap(args, w)
     t = workloads.tensors(w, "cpu")
     import oracle
     ref = oracle.RefAllocator(w.num_blocks, w.block_size, workloads.free_order(w.num_blocks, w.seed))
@@ -542,6 +547,34 @@ def run_reference_prefill(args, w):
     print(json.dumps(line))
 
 
+def run_reference_swap(args, w):
+    """The oracle's block copy between two pools, as it stands, on a bounded
+    sample of the swap workload's blocks."""
+    import oracle
+    t = workloads.tensors(w, "cpu")
+    kb = oracle.bits16(t["key_cache"][: min(w.num_blocks, 2048)])
+    dst = np.zeros_like(kb)
+    n = kb.shape[0]
+    block_bytes = kb[0].nbytes
+    prs = np.stack([np.arange(n), np.arange(n)[::-1]], 1).astype(np.int32)
+    vals = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.copy_blocks_between(dst, kb, prs)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            vals.append(n * block_bytes / dt / 1e9)
+    v = statistics.median(vals)
+    line = {"impl": "reference", "metric": SWAP_METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": n * block_bytes / (v * 1e9) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+            "config": {**w.describe(), "kernel": "oracle (C, CPU)"},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{n} blocks of {block_bytes} B per step, single thread"},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
 def run_prefill(args, rank: int, world: int):
     """One step: the copy-on-write copies of the shared prefix's last block,
     the cache write of every request's own tokens, and prompt-phase attention
@@ -673,6 +706,131 @@ def run_prefill(args, rank: int, world: int):
     print(json.dumps(line), flush=True)
 
 
+# -- swapping between the GPU pool and a pinned host pool ----------------------------------
+
+def run_swap(args, rank: int, world: int):
+    """One step: every sequence's K and V blocks swapped out to the host pool
+    and back in (two swap_blocks launches each way), the pairs planned once."""
+    import paged_kv_cache_139_gb300 as pkv
+    from paged_kv_cache_139_gb300.engine import HostKVPool, PagedKVCache
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w = make_workload(args, rank)
+    t = workloads.tensors(w, device=dev)
+    eng = PagedKVCache(w.num_blocks, w.num_kv_heads, w.head_dim, w.block_size, w.torch_dtype, dev,
+                       w.max_blocks_per_seq, workloads.free_order(w.num_blocks, w.seed),
+                       key_cache=t["key_cache"], value_cache=t["value_cache"])
+    host = HostKVPool(w.num_blocks, w.num_kv_heads, w.head_dim, w.block_size, w.torch_dtype)
+    ids = [eng.new_sequence(int(c)) for c in w.context_lens]
+    # the device copies of one round trip: plan the moves once (block ids only)
+    probe_g = pkv.BlockAllocator(w.num_blocks, w.block_size, workloads.free_order(w.num_blocks, w.seed))
+    pids = [probe_g.seq_new(int(c)) for c in w.context_lens]
+    probe_c = pkv.BlockAllocator(w.num_blocks, w.block_size)
+    cids, out_pairs = probe_g.move_group(probe_c, pids)
+    _, in_pairs = probe_c.move_group(probe_g, cids)
+    po = torch.from_numpy(out_pairs).to(dev)
+    pi = torch.from_numpy(in_pairs).to(dev)
+    nblk = out_pairs.shape[0]
+    block_bytes = w.num_kv_heads * w.block_size * w.head_dim * 2
+    moved = 2 * nblk * block_bytes                  # K and V, one direction
+    stream = torch.cuda.current_stream(dev)
+
+    def out_copy():
+        pkv.swap_blocks(host.key_cache, eng.key_cache, po, stream)
+        pkv.swap_blocks(host.value_cache, eng.value_cache, po, stream)
+
+    def in_copy():
+        pkv.swap_blocks(eng.key_cache, host.key_cache, pi, stream)
+        pkv.swap_blocks(eng.value_cache, host.value_cache, pi, stream)
+
+    clk = ClockSampler(dev.index).__enter__()
+    for _ in range(max(3, args.warmup)):
+        out_copy()
+        in_copy()
+    torch.cuda.synchronize(dev)
+    pkv.check()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    launches0 = pkv.launch_count()
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        out_copy()
+        ev[i][1].record(stream)
+        in_copy()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    launches = pkv.launch_count() - launches0
+    pkv.check()
+    t_out = statistics.fmean(a.elapsed_time(b) for a, b, _ in ev)
+    t_in = statistics.fmean(b.elapsed_time(c) for _, b, c in ev)
+    # the link's own rate: one contiguous copy of the same bytes each way (copy engine)
+    hbuf = torch.empty(moved, dtype=torch.uint8).pin_memory()
+    dbuf = torch.empty(moved, dtype=torch.uint8, device=dev)
+    ce = []
+    for i in range(3 + args.steps):
+        a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        a.record(stream)
+        hbuf.copy_(dbuf, non_blocking=True)
+        b.record(stream)
+        dbuf.copy_(hbuf, non_blocking=True)
+        c.record(stream)
+        ce.append((a, b, c))
+    torch.cuda.synchronize(dev)
+    ce_d2h = statistics.median(a.elapsed_time(b) for a, b, _ in ce[3:])
+    ce_h2d = statistics.median(b.elapsed_time(c) for _, b, c in ce[3:])
+    peak = 2 * moved / ((ce_d2h + ce_h2d) * 1e-3) / 1e9
+    # end to end through the engine: the group moves (host bookkeeping) and the copies
+    e2e_t = []
+    gids = ids
+    for i in range(args.warmup + args.steps):
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        hids, _ = eng.swap_out(gids, host)
+        gids, _ = eng.swap_in(hids, host)
+        torch.cuda.synchronize(dev)
+        if i >= args.warmup:
+            e2e_t.append(time.perf_counter() - t0)
+    pkv.check()
+    clk.__exit__(None, None, None)
+    t_e2e = statistics.fmean(e2e_t)
+    value = 2 * moved / ((t_out + t_in) * 1e-3) / 1e9
+    line = {
+        "metric": SWAP_METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_out + t_in, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u8", "kv_dtype": w.dtype, "data": "synthetic",
+        "config": {**w.describe(), "blocks_moved": nblk, "block_bytes": block_bytes,
+                   "bytes_per_direction": moved, "host_pool": "pinned host memory, addressed by the kernel"},
+        "swap_out": {"ms": t_out, "gbs": moved / (t_out * 1e-3) / 1e9},
+        "swap_in": {"ms": t_in, "gbs": moved / (t_in * 1e-3) / 1e9},
+        "roofline": {"bound": "link", "achieved": value, "peak": peak, "unit": "GB/s", "frac": value / peak,
+                     "traffic": None, "kernel": "swap_blocks",
+                     "peak_source": "one contiguous cudaMemcpyAsync of the same bytes each way, measured here",
+                     "copy_engine_d2h_gbs": moved / (ce_d2h * 1e-3) / 1e9,
+                     "copy_engine_h2d_gbs": moved / (ce_h2d * 1e-3) / 1e9},
+        "gpu_launches": launches,
+        "clocks": {**clk.summary(), "window": "warm-up + timed + e2e legs"},
+        "e2e": {"value": 2 * moved / t_e2e / 1e9, "unit": "GB/s", "h2d_bytes_per_step": moved,
+                "d2h_bytes_per_step": moved, "ms_per_step": t_e2e * 1e3,
+                "note": "engine.swap_out + swap_in: the allocator moves and the copies"},
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        kb = oracle.bits16(t["key_cache"][: min(w.num_blocks, 2048)])
+        dst = np.zeros_like(kb)
+        n = kb.shape[0]
+        prs = np.stack([np.arange(n), np.arange(n)[::-1]], 1).astype(np.int32)
+        t0 = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - t0 < 5.0:
+            oracle.copy_blocks_between(dst, kb, prs)
+            reps += 1
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": reps * n * block_bytes / dt / 1e9, "unit": "GB/s", "cores": 1,
+                                "kind": "oracle", "sample": f"{reps} x {n} blocks of {block_bytes} B copied "
+                                                            f"between two host pools, single thread, {dt:.1f} s"}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", 0))
@@ -685,6 +843,8 @@ def main():
         run_reference(args, rank, world)
     elif args.workload == "prefix":
         run_prefill(args, rank, world)
+    elif args.workload == "swap":
+        run_swap(args, rank, world)
     else:
         run_ours(args, rank, world)
     if world > 1 and args.impl == "ours":

@@ -237,6 +237,28 @@ int paged_attention_partition_size(int num_seqs, int num_heads, int num_kv_heads
 pkv_status copy_blocks(void *cache_dev, const int32_t *src_dst_pairs_dev, int num_pairs,
                        int64_t block_bytes, int num_blocks, struct CUstream_st *stream);
 
+/* ---------------------------------------------------------------------------
+ * swap_blocks -- block copies between two pools, for swapping an evicted
+ * group's blocks to the CPU and back ("vLLM & PagedAttention" §VIII and
+ * Figure 4: a GPU block allocator for the live cache, a CPU block allocator
+ * for swapped-out blocks).
+ *
+ * For each pair p: block pairs[2p+1] of dst_pool becomes a copy of block
+ * pairs[2p] of src_pool, block_bytes bytes each (the pools share the layout
+ * above).  One launch copies every pair, so small blocks cost no more
+ * transfers than large ones.  Call once for keys and once for values.
+ *   dst_pool, src_pool  [dst_blocks] / [src_blocks] blocks: device memory, or
+ *                       host memory the GPU can address (pinned, e.g.
+ *                       cudaHostAlloc), 16-byte aligned, distinct.
+ *   pairs               [num_pairs][2] int32 in device or pinned host memory;
+ *                       destinations distinct (pkv_move_group's pairs are).
+ * A block id out of range latches PKV_EINDEX and that pair is skipped.
+ * num_pairs may be 0 (nothing launched).  Asynchronous on `stream`: host
+ * buffers must stay alive until it completes.
+ * ------------------------------------------------------------------------- */
+pkv_status swap_blocks(void *dst_pool, const void *src_pool, const int32_t *pairs, int num_pairs,
+                       int64_t block_bytes, int src_blocks, int dst_blocks, struct CUstream_st *stream);
+
 /* Host-side check of a pair list: ids in range, distinct destinations, no
  * destination that is also a source.  PKV_EINVAL if any fails. */
 pkv_status pkv_validate_copy_pairs(const int32_t *src_dst_pairs_host, int num_pairs,
@@ -317,6 +339,24 @@ int pkv_block_ref(const pkv_allocator *a, int32_t block);
 int pkv_num_free(const pkv_allocator *a);
 /* Free blocks in the order they would be handed out (at most cap). */
 pkv_status pkv_free_list(const pkv_allocator *a, int32_t *out, int cap, int *n);
+
+/* Swapping ("vLLM & PagedAttention" §VIII): move the sequence group
+ * seqs[0..n-1] from allocator `src` to allocator `dst` (a GPU and a CPU pool
+ * of the same block size), all or nothing.
+ *   - The group must hold every reference to its blocks (sequences that
+ *     share blocks are evicted together); otherwise PKV_EINVAL.
+ *   - Each distinct block, in first-seen order (the sequences in the given
+ *     order, each in logical order), takes a block of `dst` with the same
+ *     reference count; pairs[2k], pairs[2k+1] = (block in src, block in
+ *     dst); *num_pairs of them (room for pairs_cap).  new_ids[i] is
+ *     seqs[i]'s id in `dst`, with the same length and a table over the new
+ *     blocks.
+ *   - Then the group is freed in `src` (sequence by sequence, as
+ *     pkv_seq_free).  The caller copies the pairs' blocks with swap_blocks
+ *     (keys and values) before any of the freed blocks is written again.
+ * Too few free blocks in `dst`: PKV_ENOMEM; on every error nothing changes. */
+pkv_status pkv_move_group(pkv_allocator *src, pkv_allocator *dst, const int32_t *seqs, int n,
+                          int32_t *new_ids, int32_t *pairs, int pairs_cap, int *num_pairs);
 
 #ifdef __cplusplus
 }

@@ -27,7 +27,7 @@ __all__ = ["PkvError", "PkvOOM", "kv_reshape_and_cache", "paged_attention_decode
            "paged_attention_decode_noalloc", "paged_attention_prefill", "paged_attention_workspace_size",
            "make_workspace",
            "paged_attention_partition_size", "copy_blocks",
-           "validate_copy_pairs", "check", "launch_count", "version", "BlockAllocator", "library_path"]
+           "validate_copy_pairs", "swap_blocks", "check", "launch_count", "version", "BlockAllocator", "library_path"]
 
 PKV_F16, PKV_BF16 = 0, 1
 
@@ -258,6 +258,31 @@ def validate_copy_pairs(pairs, num_blocks: int) -> None:
     _ck(rc, "validate_copy_pairs")
 
 
+def swap_blocks(dst_pool: torch.Tensor, src_pool: torch.Tensor, pairs: torch.Tensor,
+                stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Block pairs[p][1] of dst_pool takes block pairs[p][0] of src_pool (one
+    launch for all pairs).  Pools [NB][...] of one layout: CUDA tensors or
+    pinned host tensors; pairs int32 [n][2] on the GPU or pinned."""
+    def addr(t, name):
+        if not isinstance(t, torch.Tensor) or not (t.is_cuda or t.is_pinned()):
+            raise TypeError(f"{name} must be a CUDA tensor or pinned host memory")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        return t.data_ptr()
+    if dst_pool.shape[1:] != src_pool.shape[1:] or dst_pool.dtype != src_pool.dtype:
+        raise ValueError("swap_blocks: pools of different layouts")
+    n = pairs.shape[0] if pairs.dim() == 2 else 0
+    if n == 0:
+        return
+    if pairs.dtype != torch.int32 or pairs.shape[1] != 2:
+        raise TypeError("swap_blocks: pairs must be int32 [n][2]")
+    block_bytes = dst_pool[0].numel() * dst_pool.element_size()
+    dev = dst_pool.device if dst_pool.is_cuda else src_pool.device
+    rc = load().swap_blocks(addr(dst_pool, "dst_pool"), addr(src_pool, "src_pool"), addr(pairs, "pairs"), n,
+                            block_bytes, src_pool.shape[0], dst_pool.shape[0], _stream(stream, dev))
+    _ck(rc, "swap_blocks")
+
+
 def check(stream: Optional[torch.cuda.Stream] = None, device=None) -> None:
     """Synchronise the stream and raise if the device latched an index error
     or a wait timeout since the last check."""
@@ -338,6 +363,22 @@ class BlockAllocator:
         _ck(self._L.pkv_seq_block_table(self._h, seq, out.ctypes.data_as(ctypes.c_void_p), out.shape[0],
                                         ctypes.byref(n)), "pkv_seq_block_table")
         return out[:n.value].tolist()
+
+    def move_group(self, dst: "BlockAllocator", seqs: Sequence[int]):
+        """Move the sequence group `seqs` (holding every reference to its
+        blocks) to allocator `dst`, all or nothing: returns (new ids in dst,
+        pairs int32 [m][2] of (block here, block in dst)) for swap_blocks.
+        PkvOOM if dst has too few free blocks."""
+        s = np.ascontiguousarray(np.asarray(seqs, dtype=np.int32))
+        n = s.shape[0]
+        ids = np.empty(max(n, 1), np.int32)
+        cap = max(1, sum(len(self.block_table(int(x))) for x in s))
+        pairs = np.empty((cap, 2), np.int32)
+        npairs = ctypes.c_int()
+        _ck(self._L.pkv_move_group(self._h, dst._h, s.ctypes.data_as(ctypes.c_void_p) if n else None, n,
+                                   ids.ctypes.data_as(ctypes.c_void_p), pairs.ctypes.data_as(ctypes.c_void_p), cap,
+                                   ctypes.byref(npairs)), "pkv_move_group")
+        return ids[:n].tolist(), pairs[:npairs.value].copy()
 
     def build_block_tables(self, seqs: Sequence[int], max_blocks: int):
         """(tables int32 [n][max_blocks] padded with -1, context_lens int32 [n])."""

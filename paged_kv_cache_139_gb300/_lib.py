@@ -27,6 +27,7 @@ SIGNATURES = {
     "paged_attention_workspace_init": (_i, [_p, _sz, _p]),
     "paged_attention_partition_size": (_i, [_i, _i, _i, _i, _i, _i]),
     "copy_blocks": (_i, [_p, _p, _i, _i64, _i, _p]),
+    "swap_blocks": (_i, [_p, _p, _p, _i, _i64, _i, _i, _p]),
     "pkv_validate_copy_pairs": (_i, [_p, _i, _i]),
     "pkv_check": (_i, [_p]),
     "pkv_last_error_string": (ctypes.c_char_p, []),
@@ -46,6 +47,7 @@ SIGNATURES = {
     "pkv_block_ref": (_i, [_p, ctypes.c_int32]),
     "pkv_num_free": (_i, [_p]),
     "pkv_free_list": (_i, [_p, _p, _i, _pint]),
+    "pkv_move_group": (_i, [_p, _p, _p, _i, _p, _p, _i, _pint]),
 }
 
 STATUS = {0: "PKV_OK", 1: "PKV_EINVAL", 2: "PKV_ENOMEM", 3: "PKV_EINDEX", 4: "PKV_ECUDA", 5: "PKV_ETIMEOUT"}

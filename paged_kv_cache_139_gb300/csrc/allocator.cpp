@@ -10,6 +10,11 @@
 // "How PagedAttention changed LLM serving throughput": a sequence uses
 //   exactly ceil(len / block_size) blocks.
 //
+// Swapping ("vLLM & PagedAttention" §VIII, Figure 4): pkv_move_group moves an
+// evicted sequence group to a second allocator (the CPU pool) or back, all or
+// nothing, keeping the group's sharing; the caller copies the returned block
+// pairs on the device (swap_blocks).
+//
 // The pages leave open which free block comes next; this allocator hands out
 // blocks in a caller-given initial order and re-uses freed blocks last-in,
 // first-out (freed in the sequence's logical order).
@@ -259,6 +264,58 @@ pkv_status pkv_build_block_tables(const pkv_allocator *a, const int32_t *seqs, i
         for (int j = m; j < max_blocks; j++) row[j] = -1;
         context_lens[i] = (int32_t)s->len;
     }
+    return PKV_OK;
+}
+
+pkv_status pkv_move_group(pkv_allocator *src, pkv_allocator *dst, const int32_t *seqs, int n, int32_t *new_ids,
+                          int32_t *pairs, int pairs_cap, int *num_pairs) {
+    if (!src || !dst || src == dst || n < 0 || (n > 0 && (!seqs || !new_ids)) || !num_pairs || pairs_cap < 0 ||
+        (pairs_cap > 0 && !pairs))
+        return pkv::fail(PKV_EINVAL, "pkv_move_group: bad argument");
+    *num_pairs = 0;
+    if (src->block_size != dst->block_size)
+        return pkv::fail(PKV_EINVAL, "pkv_move_group: block sizes differ (%d and %d)", src->block_size,
+                         dst->block_size);
+    // distinct blocks in first-seen order, and how often the group uses each
+    std::vector<int32_t> uses(src->num_blocks, 0), order;
+    std::vector<char> seen_seq(src->seqs.size(), 0);
+    for (int i = 0; i < n; i++) {
+        const pkv_allocator::Seq *s = src->get(seqs[i]);
+        if (!s || seen_seq[seqs[i]]) return pkv::fail(PKV_EINVAL, "pkv_move_group: unknown or repeated sequence %d", seqs[i]);
+        seen_seq[seqs[i]] = 1;
+        for (int32_t b : s->blocks) {
+            if (uses[b]++ == 0) order.push_back(b);
+        }
+    }
+    for (int32_t b : order)
+        if (src->ref[b] != uses[b])
+            return pkv::fail(PKV_EINVAL, "pkv_move_group: block %d is shared with a sequence outside the group", b);
+    if (order.size() > dst->free_stack.size())
+        return pkv::fail(PKV_ENOMEM, "pkv_move_group: need %zu blocks in the other pool, %zu free", order.size(),
+                         dst->free_stack.size());
+    if ((int64_t)order.size() > pairs_cap)
+        return pkv::fail(PKV_EINVAL, "pkv_move_group: %zu pairs, room for %d", order.size(), pairs_cap);
+    std::vector<int32_t> remap(src->num_blocks, -1);
+    for (size_t k = 0; k < order.size(); k++) {
+        const int32_t b = order[k];
+        const int32_t c = dst->pop();
+        dst->ref[c] = uses[b];
+        remap[b] = c;
+        pairs[2 * k] = b;
+        pairs[2 * k + 1] = c;
+    }
+    for (int i = 0; i < n; i++) {
+        const pkv_allocator::Seq &s = src->seqs[seqs[i]];
+        pkv_allocator::Seq m;
+        m.live = true;
+        m.len = s.len;
+        m.blocks.reserve(s.blocks.size());
+        for (int32_t b : s.blocks) m.blocks.push_back(remap[b]);
+        new_ids[i] = (int32_t)dst->seqs.size();
+        dst->seqs.push_back(std::move(m));
+    }
+    for (int i = 0; i < n; i++) pkv_seq_free(src, seqs[i]);
+    *num_pairs = (int)order.size();
     return PKV_OK;
 }
 

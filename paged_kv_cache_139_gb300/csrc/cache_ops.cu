@@ -81,6 +81,43 @@ __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(
     }
 }
 
+// Block copies between two pools (swapping): pair p copies block pairs[p][0]
+// of src to block pairs[p][1] of dst.  Either pool (and the pairs) may be in
+// host memory the GPU can address (pinned), reached over the CPU-GPU link: one
+// launch moves every block, however small.  CTAs (x: a share of a block, y: a
+// pair, looping over pairs past gridDim.y).
+__global__ void __launch_bounds__(kCopyThreads) swap_blocks_kernel(
+    uint4 *__restrict__ dst, const uint4 *__restrict__ src, const int32_t *__restrict__ pairs, int num_pairs,
+    int64_t vecs_per_block, int64_t vecs_per_cta, int src_blocks, int dst_blocks, DeviceStatus *st) {
+    pdl_trigger();
+    pdl_wait();
+    for (int p = blockIdx.y; p < num_pairs; p += gridDim.y) {
+        const int32_t sb = pairs[2 * p];
+        const int32_t db = pairs[2 * p + 1];
+        if (sb < 0 || sb >= src_blocks || db < 0 || db >= dst_blocks) {
+            if (blockIdx.x == 0 && threadIdx.x == 0) latch(st, kFlagBadPair, (sb < 0 || sb >= src_blocks) ? sb : db);
+            continue;
+        }
+        const uint4 *s = src + (int64_t)sb * vecs_per_block;
+        uint4 *d = dst + (int64_t)db * vecs_per_block;
+        const int64_t begin = (int64_t)blockIdx.x * vecs_per_cta;
+        const int64_t end = min(begin + vecs_per_cta, vecs_per_block);
+        for (int64_t i = begin + threadIdx.x; i < end; i += (int64_t)kCopyThreads * kCopyUnroll) {
+            uint4 v[kCopyUnroll];
+#pragma unroll
+            for (int u = 0; u < kCopyUnroll; u++) {
+                const int64_t j = i + (int64_t)u * kCopyThreads;
+                if (j < end) v[u] = s[j];
+            }
+#pragma unroll
+            for (int u = 0; u < kCopyUnroll; u++) {
+                const int64_t j = i + (int64_t)u * kCopyThreads;
+                if (j < end) d[j] = v[u];
+            }
+        }
+    }
+}
+
 }  // namespace
 }  // namespace pkv
 
@@ -142,6 +179,37 @@ pkv_status copy_blocks(void *cache, const int32_t *pairs, int num_pairs, int64_t
     cudaError_t e = launch(copy_blocks_kernel, dim3((unsigned)ctas_per_pair, (unsigned)num_pairs), dim3(kCopyThreads),
                            0, stream, (uint4 *)cache, pairs, vecs, vecs_per_cta, num_blocks, st);
     if (e != cudaSuccess) return fail(PKV_ECUDA, "copy_blocks: launch: %s", cudaGetErrorString(e));
+    return PKV_OK;
+}
+
+pkv_status swap_blocks(void *dst_pool, const void *src_pool, const int32_t *pairs, int num_pairs,
+                       int64_t block_bytes, int src_blocks, int dst_blocks, struct CUstream_st *stream) {
+    using namespace pkv;
+    if (num_pairs < 0 || block_bytes <= 0 || block_bytes % 16 || src_blocks < 0 || dst_blocks < 0)
+        return fail(PKV_EINVAL, "swap_blocks: bad sizes (pairs %d, block bytes %lld, blocks %d / %d)", num_pairs,
+                    (long long)block_bytes, src_blocks, dst_blocks);
+    if (num_pairs == 0) return PKV_OK;
+    if (!dst_pool || !src_pool || !pairs) return fail(PKV_EINVAL, "swap_blocks: NULL pointer");
+    if (dst_pool == src_pool) return fail(PKV_EINVAL, "swap_blocks: source and destination pool are the same (copy_blocks)");
+    if (!aligned16(dst_pool) || !aligned16(src_pool)) return fail(PKV_EINVAL, "swap_blocks: pools must be 16-byte aligned");
+    DeviceStatus *st = status_ptr();
+    if (!st) return fail(PKV_ECUDA, "swap_blocks: no device status word");
+    const int64_t vecs = block_bytes / 16;
+    const int64_t per_iter = (int64_t)kCopyThreads * kCopyUnroll;
+    // enough CTAs that every SM has several in flight; small blocks take one CTA each
+    int64_t ctas_per_pair = (vecs + per_iter - 1) / per_iter;
+    const int64_t want = (int64_t)sm_count() * 8;
+    if (ctas_per_pair * num_pairs > want) {
+        ctas_per_pair = (want + num_pairs - 1) / num_pairs;
+        if (ctas_per_pair < 1) ctas_per_pair = 1;
+    }
+    const int64_t vecs_per_cta = (vecs + ctas_per_pair - 1) / ctas_per_pair;
+    ctas_per_pair = (vecs + vecs_per_cta - 1) / vecs_per_cta;
+    const unsigned gy = (unsigned)(num_pairs < 65535 ? num_pairs : 65535);
+    cudaError_t e = launch(swap_blocks_kernel, dim3((unsigned)ctas_per_pair, gy), dim3(kCopyThreads), 0, stream,
+                           (uint4 *)dst_pool, (const uint4 *)src_pool, pairs, num_pairs, vecs, vecs_per_cta, src_blocks,
+                           dst_blocks, st);
+    if (e != cudaSuccess) return fail(PKV_ECUDA, "swap_blocks: launch: %s", cudaGetErrorString(e));
     return PKV_OK;
 }
 

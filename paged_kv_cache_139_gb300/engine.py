@@ -20,7 +20,7 @@ import ctypes
 import math
 
 from . import (BlockAllocator, PkvError, copy_blocks, kv_reshape_and_cache, make_workspace,
-               paged_attention_decode, paged_attention_prefill, paged_attention_workspace_size)
+               paged_attention_decode, paged_attention_prefill, paged_attention_workspace_size, swap_blocks)
 from ._lib import load
 
 
@@ -66,6 +66,20 @@ class DevicePrefill:
     context_lens: torch.Tensor
     query_start: torch.Tensor
     max_query_len: int
+
+
+class HostKVPool:
+    """The CPU side of swapping ("vLLM & PagedAttention" §VIII, Fig. 4): K and
+    V pools in pinned host memory, which the GPU addresses directly, and the
+    CPU block allocator that owns them."""
+
+    def __init__(self, num_blocks: int, num_kv_heads: int, head_dim: int, block_size: int, dtype: torch.dtype,
+                 free_order: Optional[Sequence[int]] = None):
+        shape = (num_blocks, num_kv_heads, block_size, head_dim)
+        self.key_cache = torch.empty(shape, dtype=dtype, pin_memory=True)
+        self.value_cache = torch.empty(shape, dtype=dtype, pin_memory=True)
+        self.alloc = BlockAllocator(num_blocks, block_size, free_order)
+        self.num_blocks, self.block_size = num_blocks, block_size
 
 
 class PagedKVCache:
@@ -186,6 +200,31 @@ class PagedKVCache:
         return paged_attention_prefill(out, query, self.key_cache, self.value_cache, step.tables,
                                        step.context_lens, step.query_start, scale=scale,
                                        max_query_len=step.max_query_len)
+
+    # -- swapping ----------------------------------------------------------------
+    def swap_out(self, seqs: Sequence[int], host: HostKVPool, stream=None):
+        """Evict a sequence group to the host pool, all or nothing: its blocks
+        move to host blocks (one swap_blocks launch for keys, one for values)
+        and the GPU blocks are freed.  Returns the group's ids in the host
+        pool and the (GPU block, host block) pairs."""
+        ids, pairs = self.alloc.move_group(host.alloc, seqs)
+        if len(pairs):
+            p = torch.from_numpy(pairs).pin_memory()
+            swap_blocks(host.key_cache, self.key_cache, p, stream)
+            swap_blocks(host.value_cache, self.value_cache, p, stream)
+            self._keep_pairs = p            # alive until the copies are done (next sync)
+        return ids, pairs
+
+    def swap_in(self, host_seqs: Sequence[int], host: HostKVPool, stream=None):
+        """Bring a swapped-out group back: the reverse move and copies.
+        Returns the group's GPU ids and the (host block, GPU block) pairs."""
+        ids, pairs = host.alloc.move_group(self.alloc, host_seqs)
+        if len(pairs):
+            p = torch.from_numpy(pairs).pin_memory()
+            swap_blocks(self.key_cache, host.key_cache, p, stream)
+            swap_blocks(self.value_cache, host.value_cache, p, stream)
+            self._keep_pairs = p
+        return ids, pairs
 
     def prepare_prefill(self, query: torch.Tensor, key: torch.Tensor, value: torch.Tensor, step: DevicePrefill,
                         out: torch.Tensor, scale: Optional[float] = None,

@@ -137,3 +137,81 @@ def test_random_sequences_match_reference(seed):
             nat.free(s)
             live.remove(s)
         _same_state(nat, ref, live)
+
+
+def _groups(ref, rng, n):
+    """n sequence groups (a prompt and its forks, some with suffixes) on the
+    reference allocator, returned with the op script that rebuilds them."""
+    script, groups = [], []
+    for _ in range(n):
+        plen, k = int(rng.integers(1, 12)), int(rng.integers(1, 4))
+        sfx = [int(rng.integers(0, 6)) for _ in range(k)]
+        script.append((plen, k, sfx))
+    return script
+
+
+def _build(alloc, script):
+    groups = []
+    for plen, k, sfx in script:
+        root = alloc.seq_new(plen)
+        g = [root] + [alloc.fork(root) for _ in range(k - 1)]
+        for sid, n in zip(g, sfx):
+            for _ in range(n):
+                alloc.append(sid)
+        groups.append(g)
+    return groups
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
+def test_swap_moves_match_reference(seed):
+    """Random groups swapped out to a CPU pool and back in random order: both
+    pools' tables, counts, free lists and the copy pairs match the reference
+    allocator exactly; too-small pools and half groups are refused without a
+    change."""
+    rng = np.random.default_rng(seed)
+    NG, NC, B = 64, 40, 4
+    og = rng.permutation(NG).astype(np.int32)
+    oc = rng.permutation(NC).astype(np.int32)
+    ng, nc = pkv.BlockAllocator(NG, B, og), pkv.BlockAllocator(NC, B, oc)
+    rg, rc = RefAllocator(NG, B, og), RefAllocator(NC, B, oc)
+    script = _groups(rg, rng, 6)
+    gn, gr = _build(ng, script), _build(rg, script)
+    assert gn == gr
+    where = ["gpu"] * len(gn)
+    for step in range(30):
+        i = int(rng.integers(len(gn)))
+        src_n, dst_n, src_r, dst_r = (ng, nc, rg, rc) if where[i] == "gpu" else (nc, ng, rc, rg)
+        seqs = gn[i]
+        shares = any(src_r.block_ref(b) > 1 for b in src_r.block_table(seqs[0]))
+        if len(seqs) > 1 and shares and rng.random() < 0.3:
+            # half a sharing group: refused, nothing changes
+            with pytest.raises(pkv.PkvError):
+                src_n.move_group(dst_n, seqs[:1])
+            with pytest.raises(ValueError):
+                src_r.move_group(dst_r, seqs[:1])
+            continue
+        try:
+            ids_r, pairs_r = src_r.move_group(dst_r, seqs)
+        except AllocatorOOM:
+            with pytest.raises(pkv.PkvOOM):
+                src_n.move_group(dst_n, seqs)
+            continue
+        ids_n, pairs_n = src_n.move_group(dst_n, seqs)
+        assert ids_n == ids_r
+        assert [tuple(p) for p in pairs_n.tolist()] == pairs_r
+        gn[i] = ids_n
+        where[i] = "cpu" if where[i] == "gpu" else "gpu"
+        for a_n, a_r, side in ((ng, rg, "gpu"), (nc, rc, "cpu")):
+            live = [s for g, w in zip(gn, where) if w == side for s in g]
+            _same_state(a_n, a_r, live)
+
+
+def test_swap_rejects_mismatched_pools():
+    a, b = pkv.BlockAllocator(8, 4), pkv.BlockAllocator(8, 8)
+    s = a.seq_new(5)
+    with pytest.raises(pkv.PkvError):
+        a.move_group(b, [s])
+    with pytest.raises(pkv.PkvError):
+        a.move_group(a, [s])
+    with pytest.raises(pkv.PkvError):
+        a.move_group(pkv.BlockAllocator(8, 4), [s, s])

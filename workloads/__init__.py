@@ -16,6 +16,7 @@ and §VII for parallel sampling over shared prompt blocks):
   sampling    64 prompts x 4 samples over shared prompt blocks (CoW)
   longgqa     32 q-heads / 8 kv-heads, 8 seqs x 32768 tokens, bf16
   prefix      prompt phase: 32 requests after a shared 1000-token prefix
+  swap        32 Llama-2-7B-layer sequences swapped to a CPU pool and back
 
 The pages give no length distribution for real traffic (their ShareGPT and
 Alpaca traces are not available here); the lognormal and uniform models below
@@ -220,9 +221,24 @@ def prefix(num_requests: int = 32, prefix_len: int = 1000, min_own: int = 64, ma
                     query_lens=own, prefix_len=prefix_len)
 
 
+def swap(block_size: int = 16, num_seqs: int = 32, min_ctx: int = 512, max_ctx: int = 4096,
+         seed: int = BASE_SEED * 1000 + 7) -> Workload:
+    """Swapping ("vLLM & PagedAttention" §VIII): a batch of Llama-2-7B-layer
+    sequences (32 x 128 MHA, f16), contexts uniform[min_ctx, max_ctx], all
+    evicted to a CPU pool of the same size and brought back; the block size
+    is the ablation's variable (§XII)."""
+    rng = _rng(seed)
+    ctx = uniform_lengths(rng, min_ctx, max_ctx, num_seqs)
+    nb = int(sum(_ceil_div(int(c), block_size) for c in ctx))
+    return Workload(f"swap: {num_seqs} seqs, MHA 32x128, B={block_size}, ctx uniform[{min_ctx},{max_ctx}], f16",
+                    num_seqs=num_seqs, num_heads=32, num_kv_heads=32, head_dim=128, block_size=block_size,
+                    dtype="f16", context_lens=ctx, max_blocks_per_seq=_ceil_div(max_ctx, block_size),
+                    num_blocks=nb, seed=seed + block_size)
+
+
 def by_name(name: str, **kw) -> Workload:
     table = {"tiny": tiny, "opt13b": opt13b, "llama7b": llama7b,
-             "sampling": sampling, "longgqa": longgqa, "prefix": prefix}
+             "sampling": sampling, "longgqa": longgqa, "prefix": prefix, "swap": swap}
     return table[name](**kw)
 
 
