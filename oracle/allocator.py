@@ -20,6 +20,13 @@ Rules and their sources:
     reaches zero returns to the pool ("vLLM & PagedAttention" §VII, Fig. 9).
   * fork, append and free are the three sequence primitives ("vLLM &
     PagedAttention" §X).
+  * Beam search ("vLLM & PagedAttention" §VII and Fig. 9): one step turns
+    the current candidates into the next set.  Every new candidate names its
+    parent; the parent's first child continues the parent's sequence, each
+    further child forks it; every new candidate then appends its token (a
+    write into a shared partly filled block copies that one block); parents
+    nobody chose are pruned last, and blocks only they held return to the
+    pool.  All or nothing.
   * Swapping ("vLLM & PagedAttention" §VIII and Fig. 4): the blocks of an
     evicted sequence group move to a second (CPU) allocator and back.  A
     group leaves all together or not at all; sequences that share blocks go
@@ -129,6 +136,45 @@ class RefAllocator:
             self.ref[b] -= 1
             if self.ref[b] == 0:
                 self._free.append(b)
+
+    # -- beam search ---------------------------------------------------------
+    def beam_step(self, beams, parents):
+        """One beam-search step: new candidate i continues beams[parents[i]].
+        Returns (new beam ids, slots of their new tokens, copy-on-write
+        pairs); raises AllocatorOOM with nothing changed."""
+        beams = [int(b) for b in beams]
+        parents = [int(p) for p in parents]
+        if len(set(beams)) != len(beams) or any(b not in self._seqs for b in beams):
+            raise ValueError("unknown or repeated beam")
+        if any(p < 0 or p >= len(beams) for p in parents):
+            raise ValueError("parent index out of range")
+        snapshot = (list(self.ref), list(self._free), self._next_id,
+                    {k: {"blocks": list(v["blocks"]), "len": v["len"]} for k, v in self._seqs.items()})
+        taken = [False] * len(beams)
+        new = []
+        for p in parents:
+            if not taken[p]:
+                taken[p] = True
+                new.append(beams[p])
+            else:
+                new.append(self.fork(beams[p]))
+        slots, pairs = [], []
+        try:
+            for b in new:
+                slot, cow = self.append(b)
+                slots.append(slot)
+                if cow is not None:
+                    pairs.append(cow)
+        except AllocatorOOM:
+            self.ref, self._free, self._next_id, self._seqs = snapshot
+            raise
+        for i, b in enumerate(beams):
+            if not taken[i]:
+                self.free(b)
+        return new, slots, pairs
+
+    def blocks_in_use(self) -> int:
+        return self.num_blocks - len(self._free)
 
     # -- swapping between pools ---------------------------------------------
     def move_group(self, dst: "RefAllocator", seqs):

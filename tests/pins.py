@@ -465,6 +465,84 @@ def pin_prefill_which_subset():
     assert np.isnan(part[1, 1]).all()
 
 
+# -- beam search ------------------------------------------------------------------
+
+def _fig9_tree():
+    """Candidates A=[0,1,3,6], B=[0,1,3,7], C=[0,2,4,8], D=[0,1,5] (block size
+    2, every block full), built with fork/append in block-id order."""
+    a = oracle.RefAllocator(16, 2)
+    C = a.seq_new(2)
+    A = a.fork(C)
+    a.append(A); a.append(A)
+    a.append(C); a.append(C)
+    D = a.fork(A)
+    a.append(A); a.append(A)
+    Bc = a.fork(A)
+    a.append(C); a.append(C)
+    a.append(D); a.append(D)
+    a.append(A); a.append(A)
+    a.append(Bc); a.append(Bc)
+    a.append(C); a.append(C)
+    return a, [A, Bc, C, D]
+
+
+def pin_beam_step_fig9():
+    """The width-4 step of the pages' Figure 9: survivors A and B each branch
+    in two, C and D are pruned; the four survivors grow into new blocks 9-12
+    and the blocks only C and D held (2, 4, 5, 8) return to the pool, while
+    block 0 stays shared by all."""
+    g = golden("beam_prune_fig9.json")
+    a, (A, Bc, C, D) = _fig9_tree()
+    new, slots, pairs = a.beam_step([A, Bc, C, D], [0, 0, 1, 1])
+    assert new[0] == A and new[2] == Bc and len(set(new)) == 4 and not pairs
+    assert [a.block_table(s)[-1] for s in new] == g["new_for_survivors"]
+    assert sorted(a.free_list()[:4]) == g["freed_on_prune"]
+    assert all(a.block_ref(b) == 0 for b in g["freed_on_prune"])
+    assert a.block_ref(g["shared_by_all"]) == 4
+    assert slots == [b * 2 for b in g["new_for_survivors"]]
+
+
+def pin_beam_step_single_block_copy():
+    """Children of one parent writing into its shared, partly filled last
+    block: every child but the last copies that one block (the last writes in
+    place); full shared blocks are never copied."""
+    a = oracle.RefAllocator(16, 4)
+    p = a.seq_new(6)                           # [b0 full, b1 with 2 of 4]
+    b0, b1 = a.block_table(p)
+    new, slots, pairs = a.beam_step([p], [0, 0, 0])
+    assert len(pairs) == 2 and all(src == b1 for src, _ in pairs)
+    tabs = [a.block_table(s) for s in new]
+    assert all(t[0] == b0 for t in tabs) and a.block_ref(b0) == 3
+    assert sorted(t[1] for t in tabs) == sorted([b1] + [d for _, d in pairs])
+    assert a.block_ref(b1) == 1 and all(s % 4 == 2 for s in slots)
+
+
+def pin_beam_step_all_or_nothing():
+    a = oracle.RefAllocator(3, 2)
+    p = a.seq_new(3)                            # 2 blocks, 1 free
+    before = _alloc_state(a), a._next_id
+    try:
+        a.beam_step([p], [0, 0, 0])             # needs two copies
+        raise AssertionError("a step without room went through")
+    except oracle.AllocatorOOM:
+        pass
+    assert (_alloc_state(a), a._next_id) == before
+
+
+def pin_beam_memory_closed_form():
+    """k beams sharing a P-block prompt, each with its own t-block tail: the
+    pool holds P + k t blocks, k (P + t) without sharing."""
+    B, P, t, k = 4, 5, 3, 4
+    a = oracle.RefAllocator(64, B)
+    root = a.seq_new(P * B)
+    beams = [root] + [a.fork(root) for _ in range(k - 1)]
+    for _ in range(t * B):
+        beams, _, _ = a.beam_step(beams, list(range(k)))
+    used = a.blocks_in_use()
+    unshared = sum(-(-a.seq_len(b) // B) for b in beams)
+    assert used == P + k * t and unshared == k * (P + t)
+
+
 # -- swapping between a GPU and a CPU pool ------------------------------------------
 
 def _alloc_state(a):
