@@ -41,6 +41,7 @@ import workloads  # noqa: E402
 
 METRIC = "paged decode attention effective KV-read GB/s and % of GB300 HBM peak"
 PREFILL_METRIC = "prompt-phase paged attention TFLOP/s (causal, after a shared prefix)"
+BEAM_METRIC = "beam-search decode effective KV-read GB/s (all beams, shared blocks counted per beam)"
 SWAP_METRIC = "swap GB/s (KV blocks GPU -> pinned host -> GPU, both directions)"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -54,7 +55,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="opt13b",
-                    choices=["tiny", "opt13b", "llama7b", "sampling", "longgqa", "prefix", "swap"])
+                    choices=["tiny", "opt13b", "llama7b", "sampling", "longgqa", "prefix", "swap", "beam"])
+    ap.add_argument("--beam-width", type=int, default=4)
     ap.add_argument("--block-size", type=int, default=16)
     ap.add_argument("--head-dim", type=int, default=128, choices=[64, 128])
     ap.add_argument("--partition-size", type=int, default=-1)
@@ -70,6 +72,8 @@ def make_workload(args, rank: int) -> workloads.Workload:
         kw["head_dim"] = args.head_dim
     if args.workload == "swap":
         kw["block_size"] = args.block_size
+    if args.workload == "beam":
+        kw["width"] = args.beam_width
     w = workloads.by_name(args.workload, **kw)
     if rank:
         w = workloads.by_name(args.workload, seed=w.seed + 7919 * rank, **kw) if args.workload != "tiny" else w
@@ -706,6 +710,107 @@ def run_prefill(args, rank: int, world: int):
     print(json.dumps(line), flush=True)
 
 
+# -- beam search --------------------------------------------------------------------------
+
+def run_beam(args, rank: int, world: int):
+    """A beam search over every request: each step plans the next beams on
+    the host (fork / prune / copy-on-write), then the device copies the
+    written shared blocks, writes the new tokens and runs decode attention
+    over all beams.  The search first runs `steps0` untimed steps so that
+    the beams' histories branch and share."""
+    import paged_kv_cache_139_gb300 as pkv
+    from paged_kv_cache_139_gb300.engine import PagedKVCache
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w = make_workload(args, rank)
+    k = w.samples_per_prompt
+    B = w.block_size
+    rng = np.random.default_rng(w.seed)
+    kc = workloads.normal((w.num_blocks, w.num_kv_heads, B, w.head_dim), w.dtype, w.seed + 14, dev)
+    vc = workloads.normal((w.num_blocks, w.num_kv_heads, B, w.head_dim), w.dtype, w.seed + 15, dev)
+    eng = PagedKVCache(w.num_blocks, w.num_kv_heads, w.head_dim, B, w.torch_dtype, dev, w.max_blocks_per_seq,
+                       workloads.free_order(w.num_blocks, w.seed), key_cache=kc, value_cache=vc)
+    beams = [[eng.new_sequence(int(p_))] for p_ in w.context_lens]
+    nq = w.num_seqs * k
+    q = workloads.normal((nq, w.num_heads, w.head_dim), w.dtype, w.seed + 11, dev)
+    key = workloads.normal((nq, w.num_kv_heads, w.head_dim), w.dtype, w.seed + 12, dev)
+    value = workloads.normal((nq, w.num_kv_heads, w.head_dim), w.dtype, w.seed + 13, dev)
+    out = torch.empty_like(q)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def host_step():
+        all_new, slots, pairs = [], [], []
+        for r in range(w.num_seqs):
+            par = workloads.beam_parents(rng, len(beams[r]), k)
+            new, sl, pr = eng.alloc.beam_step(beams[r], par)
+            beams[r] = new
+            all_new += new
+            slots.append(sl)
+            pairs.append(pr)
+        s_ = np.asarray(all_new, np.int32)
+        tables, ctx = eng.alloc.build_block_tables(s_, w.max_blocks_per_seq)
+        from paged_kv_cache_139_gb300.engine import StepPlan
+        return StepPlan(s_, np.concatenate(slots), np.concatenate(pairs).reshape(-1, 2).astype(np.int32), tables, ctx)
+
+    def memory():
+        used = eng.alloc.blocks_in_use()
+        unshared = sum(-(-eng.alloc.seq_len(b) // B) for g in beams for b in g)
+        return used, unshared
+
+    steps0 = 64
+    mem_trace, host_ms, dev_ms, kvb = [], [], [], []
+    launches = 0
+    clk = ClockSampler(dev.index).__enter__()
+    for i in range(steps0 + args.warmup + args.steps):
+        t0 = time.perf_counter()
+        plan = host_step()
+        t_host = time.perf_counter() - t0
+        step = eng.upload(plan)
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        l0 = pkv.launch_count()
+        a.record(stream)
+        eng.copy_on_write(step.pairs)
+        eng.write(key, value, step.slots)
+        eng.attend(q, step, out=out)
+        b.record(stream)
+        if i >= steps0 + args.warmup:
+            torch.cuda.synchronize(dev)
+            launches += pkv.launch_count() - l0
+            dev_ms.append(a.elapsed_time(b))
+            host_ms.append(t_host * 1e3)
+            kvb.append(int(plan.context_lens.astype(np.int64).sum()) * w.kv_bytes_per_token)
+            mem_trace.append(memory())
+    torch.cuda.synchronize(dev)
+    pkv.check()
+    clk.__exit__(None, None, None)
+    used = np.array([m[0] for m in mem_trace], np.float64)
+    unshared = np.array([m[1] for m in mem_trace], np.float64)
+    t_dev = statistics.fmean(dev_ms)
+    value = statistics.fmean(kvb) / (t_dev * 1e-3) / 1e9
+    peak, peak_src = hbm_peak()
+    line = {
+        "metric": BEAM_METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_dev, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "kv_dtype": w.dtype, "data": "synthetic",
+        "config": {**w.describe(), "beam_width": k, "beams": nq, "untimed_steps_before": steps0 + args.warmup,
+                   "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB memset, outside the timed events)"},
+        "memory": {"blocks_in_use": float(used.mean()), "blocks_without_sharing": float(unshared.mean()),
+                   "saving_pct": float(100.0 * (1.0 - used.sum() / unshared.sum())),
+                   "note": "blocks held with block sharing vs every beam holding its own copy of its history"},
+        "host_beam_step_ms": statistics.fmean(host_ms),
+        "roofline": {"bound": "hbm", "achieved": value, "peak": peak, "unit": "GB/s", "frac": value / peak,
+                     "traffic": None, "kernel": "copy_blocks + kv_reshape_and_cache + paged_attention_decode",
+                     "peak_source": f"{peak_src}", "note": "shared prompt blocks are read once per beam; L2 serves the repeats"},
+        "gpu_launches": launches,
+        "clocks": {**clk.summary(), "window": "the whole search"},
+        "e2e": None,
+    }
+    print(json.dumps(line), flush=True)
+
+
 # -- swapping between the GPU pool and a pinned host pool ----------------------------------
 
 def run_swap(args, rank: int, world: int):
@@ -845,6 +950,8 @@ def main():
         run_prefill(args, rank, world)
     elif args.workload == "swap":
         run_swap(args, rank, world)
+    elif args.workload == "beam":
+        run_beam(args, rank, world)
     else:
         run_ours(args, rank, world)
     if world > 1 and args.impl == "ours":

@@ -340,6 +340,22 @@ int pkv_num_free(const pkv_allocator *a);
 /* Free blocks in the order they would be handed out (at most cap). */
 pkv_status pkv_free_list(const pkv_allocator *a, int32_t *out, int cap, int *n);
 
+/* One beam-search step ("vLLM & PagedAttention" §VII, Figure 9): the kn new
+ * candidates continue beams[parents[i]] (0 <= parents[i] < k).
+ *   - The first candidate naming a parent continues the parent's sequence
+ *     (new_beams[i] = that id); each further one forks it (a new id).
+ *   - Every candidate then appends one token, in order: slots[i] receives its
+ *     slot; a write into a shared, partly filled last block copies that block
+ *     first (cow_pairs gets (src, dst); room for kn pairs, *num_pairs of
+ *     them).
+ *   - Beams no candidate names are freed last.
+ * All or nothing: PKV_ENOMEM (too few free blocks) or PKV_EINVAL (unknown
+ * or repeated beam, bad parent index) change nothing. */
+pkv_status pkv_beam_step(pkv_allocator *a, const int32_t *beams, int k, const int32_t *parents, int kn,
+                         int32_t *new_beams, int64_t *slots, int32_t *cow_pairs, int *num_pairs);
+/* Blocks currently held by some sequence (num_blocks - free). */
+int pkv_blocks_in_use(const pkv_allocator *a);
+
 /* Swapping ("vLLM & PagedAttention" §VIII): move the sequence group
  * seqs[0..n-1] from allocator `src` to allocator `dst` (a GPU and a CPU pool
  * of the same block size), all or nothing.

@@ -364,6 +364,28 @@ class BlockAllocator:
                                         ctypes.byref(n)), "pkv_seq_block_table")
         return out[:n.value].tolist()
 
+    def beam_step(self, beams: Sequence[int], parents: Sequence[int]):
+        """One beam-search step: new candidate i continues beams[parents[i]]
+        (the first child continues the sequence, later ones fork it; all
+        append a token; unchosen beams are freed).  Returns (new beam ids,
+        slots int64 [kn], copy-on-write pairs int32 [m][2]); PkvOOM leaves
+        everything unchanged."""
+        b = np.ascontiguousarray(np.asarray(beams, dtype=np.int32))
+        p = np.ascontiguousarray(np.asarray(parents, dtype=np.int32))
+        kn = p.shape[0]
+        new = np.empty(max(kn, 1), np.int32)
+        slots = np.empty(max(kn, 1), np.int64)
+        pairs = np.empty((max(kn, 1), 2), np.int32)
+        npairs = ctypes.c_int()
+        _ck(self._L.pkv_beam_step(self._h, b.ctypes.data_as(ctypes.c_void_p) if b.size else None, b.shape[0],
+                                  p.ctypes.data_as(ctypes.c_void_p) if kn else None, kn,
+                                  new.ctypes.data_as(ctypes.c_void_p), slots.ctypes.data_as(ctypes.c_void_p),
+                                  pairs.ctypes.data_as(ctypes.c_void_p), ctypes.byref(npairs)), "pkv_beam_step")
+        return new[:kn].tolist(), slots[:kn].copy(), pairs[:npairs.value].copy()
+
+    def blocks_in_use(self) -> int:
+        return self._L.pkv_blocks_in_use(self._h)
+
     def move_group(self, dst: "BlockAllocator", seqs: Sequence[int]):
         """Move the sequence group `seqs` (holding every reference to its
         blocks) to allocator `dst`, all or nothing: returns (new ids in dst,

@@ -48,6 +48,8 @@ SIGNATURES = {
     "pkv_num_free": (_i, [_p]),
     "pkv_free_list": (_i, [_p, _p, _i, _pint]),
     "pkv_move_group": (_i, [_p, _p, _p, _i, _p, _p, _i, _pint]),
+    "pkv_beam_step": (_i, [_p, _p, _i, _p, _i, _p, _p, _p, _pint]),
+    "pkv_blocks_in_use": (_i, [_p]),
 }
 
 STATUS = {0: "PKV_OK", 1: "PKV_EINVAL", 2: "PKV_ENOMEM", 3: "PKV_EINDEX", 4: "PKV_ECUDA", 5: "PKV_ETIMEOUT"}

@@ -10,6 +10,11 @@
 // "How PagedAttention changed LLM serving throughput": a sequence uses
 //   exactly ceil(len / block_size) blocks.
 //
+// Beam search ("vLLM & PagedAttention" §VII, Figure 9): pkv_beam_step turns
+// the current candidates into the next set with fork / append / free (the
+// first child of a parent continues its sequence, later children fork it,
+// every child appends its token, parents nobody chose are freed last).
+//
 // Swapping ("vLLM & PagedAttention" §VIII, Figure 4): pkv_move_group moves an
 // evicted sequence group to a second allocator (the CPU pool) or back, all or
 // nothing, keeping the group's sharing; the caller copies the returned block
@@ -266,6 +271,64 @@ pkv_status pkv_build_block_tables(const pkv_allocator *a, const int32_t *seqs, i
     }
     return PKV_OK;
 }
+
+pkv_status pkv_beam_step(pkv_allocator *a, const int32_t *beams, int k, const int32_t *parents, int kn,
+                         int32_t *new_beams, int64_t *slots, int32_t *cow_pairs, int *num_pairs) {
+    if (!a || k < 0 || kn < 0 || (k > 0 && !beams) || (kn > 0 && (!parents || !new_beams || !slots || !cow_pairs)) ||
+        !num_pairs)
+        return pkv::fail(PKV_EINVAL, "pkv_beam_step: bad argument");
+    *num_pairs = 0;
+    std::vector<char> seen(a->seqs.size(), 0);
+    for (int i = 0; i < k; i++) {
+        if (!a->get(beams[i]) || seen[beams[i]])
+            return pkv::fail(PKV_EINVAL, "pkv_beam_step: unknown or repeated beam %d", beams[i]);
+        seen[beams[i]] = 1;
+    }
+    for (int i = 0; i < kn; i++)
+        if (parents[i] < 0 || parents[i] >= k)
+            return pkv::fail(PKV_EINVAL, "pkv_beam_step: parent index %d of candidate %d out of range", parents[i], i);
+    const size_t nseq0 = a->seqs.size();
+    std::vector<char> taken(k, 0);
+    for (int i = 0; i < kn; i++) {
+        const int p = parents[i];
+        if (!taken[p]) {
+            taken[p] = 1;
+            new_beams[i] = beams[p];
+        } else {
+            pkv_status st = pkv_seq_fork(a, beams[p], &new_beams[i]);
+            if (st != PKV_OK) return st;           // cannot happen: the parent is live
+        }
+    }
+    std::vector<AppendUndo> log;
+    log.reserve(kn);
+    int np = 0;
+    for (int i = 0; i < kn; i++) {
+        int32_t src, dst;
+        AppendUndo u;
+        pkv_status st = append_one(a, new_beams[i], &slots[i], &src, &dst, &u);
+        if (st != PKV_OK) {
+            // undo the appends, then the forks (children take the newest ids)
+            for (int j = (int)log.size() - 1; j >= 0; j--) undo_append(a, log[j]);
+            while (a->seqs.size() > nseq0) {
+                for (int32_t b : a->seqs.back().blocks) a->ref[b] -= 1;
+                a->seqs.pop_back();
+            }
+            return st;
+        }
+        log.push_back(u);
+        if (src >= 0) {
+            cow_pairs[2 * np] = src;
+            cow_pairs[2 * np + 1] = dst;
+            np++;
+        }
+    }
+    for (int i = 0; i < k; i++)
+        if (!taken[i]) pkv_seq_free(a, beams[i]);
+    *num_pairs = np;
+    return PKV_OK;
+}
+
+int pkv_blocks_in_use(const pkv_allocator *a) { return a ? a->num_blocks - (int)a->free_stack.size() : -1; }
 
 pkv_status pkv_move_group(pkv_allocator *src, pkv_allocator *dst, const int32_t *seqs, int n, int32_t *new_ids,
                           int32_t *pairs, int pairs_cap, int *num_pairs) {

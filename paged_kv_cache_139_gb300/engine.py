@@ -116,6 +116,15 @@ class PagedKVCache:
         tables, ctx = self.alloc.build_block_tables(s, self.max_blocks_per_seq)
         return StepPlan(s, slots, pairs, tables, ctx)
 
+    def plan_beam_step(self, beams: Sequence[int], parents: Sequence[int]) -> StepPlan:
+        """One beam-search step on the host: new candidate i continues
+        beams[parents[i]] (fork where a parent has several children, prune
+        the rest), each appends its token; the plan holds the new beams."""
+        new, slots, pairs = self.alloc.beam_step(beams, parents)
+        s = np.asarray(new, dtype=np.int32)
+        tables, ctx = self.alloc.build_block_tables(s, self.max_blocks_per_seq)
+        return StepPlan(s, slots, pairs, tables, ctx)
+
     def plan_tables(self, seqs: Sequence[int]) -> StepPlan:
         """Tables of the sequences as they stand (no new token)."""
         s = np.asarray(seqs, dtype=np.int32)

@@ -215,3 +215,65 @@ def test_swap_rejects_mismatched_pools():
         a.move_group(a, [s])
     with pytest.raises(pkv.PkvError):
         a.move_group(pkv.BlockAllocator(8, 4), [s, s])
+
+
+def test_beam_step_fig9():
+    """The pages' Figure 9 step, natively: blocks 9-12 for the survivors, 2,
+    4, 5, 8 back in the pool."""
+    g = golden("beam_prune_fig9.json")
+    a = pkv.BlockAllocator(16, 2)
+    C = a.seq_new(2)
+    A = a.fork(C)
+    a.append(A); a.append(A)
+    a.append(C); a.append(C)
+    D = a.fork(A)
+    a.append(A); a.append(A)
+    Bc = a.fork(A)
+    a.append(C); a.append(C)
+    a.append(D); a.append(D)
+    a.append(A); a.append(A)
+    a.append(Bc); a.append(Bc)
+    a.append(C); a.append(C)
+    new, slots, pairs = a.beam_step([A, Bc, C, D], [0, 0, 1, 1])
+    assert [a.block_table(s)[-1] for s in new] == g["new_for_survivors"] and len(pairs) == 0
+    assert sorted(a.free_list()[:4]) == g["freed_on_prune"]
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_beam_search_matches_reference(seed):
+    """Random beam searches (width 2-6, random parent choices, pools small
+    enough to run out): every step's ids, slots, copy pairs, tables, counts and
+    free lists match the reference allocator, and an out-of-blocks step
+    changes nothing on either side."""
+    rng = np.random.default_rng(seed)
+    NB, B = 48, 4
+    order = rng.permutation(NB).astype(np.int32)
+    nat, ref = pkv.BlockAllocator(NB, B, order), RefAllocator(NB, B, order)
+    width = int(rng.integers(2, 7))
+    plen = int(rng.integers(1, 20))
+    beams_n = [nat.seq_new(plen)]
+    beams_r = [ref.seq_new(plen)]
+    ooms = 0
+    for step in range(60):
+        kn = width if step else width
+        parents = rng.integers(0, len(beams_r), size=kn)
+        parents = np.minimum(parents, rng.integers(0, len(beams_r), size=kn))   # favour low ranks
+        try:
+            new_r, slots_r, pairs_r = ref.beam_step(beams_r, parents)
+        except AllocatorOOM:
+            with pytest.raises(pkv.PkvOOM):
+                nat.beam_step(beams_n, parents)
+            ooms += 1
+            _same_state(nat, ref, beams_r)
+            # make room: drop the last beam on both sides
+            nat.free(beams_n.pop())
+            ref.free(beams_r.pop())
+            if not beams_r:
+                break
+            continue
+        new_n, slots_n, pairs_n = nat.beam_step(beams_n, parents)
+        assert new_n == new_r and slots_n.tolist() == slots_r
+        assert [tuple(p) for p in pairs_n.tolist()] == pairs_r
+        beams_n, beams_r = new_n, new_r
+        _same_state(nat, ref, beams_r)
+        assert nat.blocks_in_use() == ref.blocks_in_use()

@@ -17,6 +17,7 @@ and §VII for parallel sampling over shared prompt blocks):
   longgqa     32 q-heads / 8 kv-heads, 8 seqs x 32768 tokens, bf16
   prefix      prompt phase: 32 requests after a shared 1000-token prefix
   swap        32 Llama-2-7B-layer sequences swapped to a CPU pool and back
+  beam        16 OPT-13B-layer requests searched with 2-6 beams
 
 The pages give no length distribution for real traffic (their ShareGPT and
 Alpaca traces are not available here); the lognormal and uniform models below
@@ -236,9 +237,38 @@ def swap(block_size: int = 16, num_seqs: int = 32, min_ctx: int = 512, max_ctx: 
                     num_blocks=nb, seed=seed + block_size)
 
 
+def beam(width: int = 4, num_requests: int = 16, steps: int = 192, seed: int = BASE_SEED * 1000 + 8) -> Workload:
+    """Beam search ("vLLM & PagedAttention" §VII, Fig. 9; §XII Fig. 15 for
+    widths 2 to 6): OPT-13B-layer requests (40 x 128 MHA, f16, B=16) with
+    lognormal(160) prompts, each searched with `width` beams for `steps`
+    tokens.  context_lens holds the prompts; parents are drawn by
+    beam_parents."""
+    rng = _rng(seed)
+    prompt = lognormal_lengths(rng, 160.0, num_requests)
+    prompt = np.clip(prompt, 1, 1024)
+    B = 16
+    max_len = int(prompt.max()) + steps + 1
+    # room for every beam's own copy of everything (the unshared bound) plus slack
+    nb = int(sum(width * _ceil_div(int(p_) + steps + 1, B) for p_ in prompt)) + 64
+    return Workload(f"beam: {num_requests} requests x width {width}, OPT-13B layer (MHA 40x128), B=16, "
+                    f"prompt lognormal(160), {steps} steps, f16",
+                    num_seqs=num_requests, num_heads=40, num_kv_heads=40, head_dim=128, block_size=B, dtype="f16",
+                    context_lens=prompt, max_blocks_per_seq=_ceil_div(max_len, B), num_blocks=nb, seed=seed + width,
+                    samples_per_prompt=width)
+
+
+def beam_parents(rng: np.random.Generator, k: int, width: int) -> np.ndarray:
+    """Parents of the next `width` candidates among k current beams (ranked
+    best first): the better of two uniform draws, so strong beams tend to
+    branch and weak ones to die."""
+    a = rng.integers(0, k, size=width)
+    b = rng.integers(0, k, size=width)
+    return np.sort(np.minimum(a, b)).astype(np.int32)
+
+
 def by_name(name: str, **kw) -> Workload:
     table = {"tiny": tiny, "opt13b": opt13b, "llama7b": llama7b,
-             "sampling": sampling, "longgqa": longgqa, "prefix": prefix, "swap": swap}
+             "sampling": sampling, "longgqa": longgqa, "prefix": prefix, "swap": swap, "beam": beam}
     return table[name](**kw)
 
 
