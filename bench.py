@@ -908,7 +908,9 @@ def run_swap(args, rank: int, world: int):
         "swap_out": {"ms": t_out, "gbs": moved / (t_out * 1e-3) / 1e9},
         "swap_in": {"ms": t_in, "gbs": moved / (t_in * 1e-3) / 1e9},
         "roofline": {"bound": "link", "achieved": value, "peak": peak, "unit": "GB/s", "frac": value / peak,
-                     "traffic": None, "kernel": "swap_blocks",
+                     "traffic": profile_traffic("swap", pkv.version()) if w.block_size == 16 else None,
+                     "traffic_note": "DRAM bytes of one device-to-host launch (keys), from profiles/",
+                     "kernel": "swap_blocks",
                      "peak_source": "one contiguous cudaMemcpyAsync of the same bytes each way, measured here",
                      "copy_engine_d2h_gbs": moved / (ce_d2h * 1e-3) / 1e9,
                      "copy_engine_h2d_gbs": moved / (ce_h2d * 1e-3) / 1e9},
