@@ -68,6 +68,68 @@ class DevicePrefill:
     max_query_len: int
 
 
+class StagedInputs:
+    """A step's host inputs in one pinned buffer and their device copies in one
+    device buffer, laid out alike (each tensor 256-byte aligned): a step then
+    moves all its inputs with a single host-to-device copy instead of one per
+    tensor.  Write the step's inputs into `host[name]`, call `upload()`, and
+    pass `dev[name]` to the device calls."""
+
+    def __init__(self, specs, device):
+        """specs: {name: (shape, dtype)}."""
+        self.device = torch.device(device)
+        offs, off = {}, 0
+        for name, (shape, dtype) in specs.items():
+            n = int(np.prod(shape)) * torch.tensor([], dtype=dtype).element_size()
+            offs[name] = (off, n, tuple(shape), dtype)
+            off += (n + 255) // 256 * 256
+        self.nbytes = off
+        self._hbuf = torch.empty(max(off, 1), dtype=torch.uint8).pin_memory()
+        self._dbuf = torch.empty(max(off, 1), dtype=torch.uint8, device=self.device)
+        view = lambda buf, o, n, shape, dt: buf[o:o + n].view(dt).view(shape)
+        self.host = {k: view(self._hbuf, *v) for k, v in offs.items()}
+        self.dev = {k: view(self._dbuf, *v) for k, v in offs.items()}
+
+    def upload(self, stream: Optional[torch.cuda.Stream] = None) -> None:
+        """One asynchronous copy of every input (on `stream`, default current)."""
+        s = stream or torch.cuda.current_stream(self.device)
+        with torch.cuda.stream(s):
+            self._dbuf.copy_(self._hbuf, non_blocking=True)
+
+
+class GraphStep:
+    """A whole step -- one staged upload of its inputs, its device calls, the
+    read-back of its output -- captured once in a CUDA graph and replayed:
+    the GPU runs the copies and kernels back to back with no host round trip
+    between them.  `prepare(stream)` must build the device calls (for example
+    PagedKVCache.prepare / prepare_prefill) on the stream it is given, with
+    the staged inputs' device views as arguments; the buffers must stay fixed
+    (their contents may change between replays)."""
+
+    def __init__(self, staged: StagedInputs, prepare, out: torch.Tensor, host_out: torch.Tensor, warmup: int = 2):
+        dev = staged.device
+        self._stream = torch.cuda.Stream(dev)
+        self._prep = prepare(self._stream)
+        self._staged, self._out, self._host_out = staged, out, host_out
+        self._stream.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(self._stream):
+            for _ in range(warmup):                  # first launches configure the kernels
+                self._body()
+        self._stream.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=self._stream):
+            self._body()
+        self.device = dev
+
+    def _body(self):
+        self._staged.upload(self._stream)
+        self._prep()
+        self._host_out.copy_(self._out, non_blocking=True)
+
+    def replay(self) -> None:
+        self.graph.replay()
+
+
 class HostKVPool:
     """The CPU side of swapping ("vLLM & PagedAttention" §VIII, Fig. 4): K and
     V pools in pinned host memory, which the GPU addresses directly, and the

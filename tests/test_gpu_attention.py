@@ -269,3 +269,55 @@ def test_prepared_step_matches_decode(cuda_device):
     pkv.check()
     assert pkv.launch_count() - before == 2
     assert torch.equal(out, c.out)
+
+
+def test_staged_inputs_single_upload(cuda_device):
+    """A decode step whose inputs arrive through one pinned staging buffer (one
+    host-to-device copy) gives the same output as separately uploaded ones."""
+    from paged_kv_cache_139_gb300.engine import StagedInputs
+    w = _custom(H=8, Hkv=2, ctx=(5, 300, 1000, 77), S=4)
+    c = Case(w, cuda_device)
+    plan, eng = c.plan, c.eng
+    src = {"q": c.query, "key": c.key, "value": c.value, "slots": torch.from_numpy(plan.slots),
+           "tables": torch.from_numpy(plan.tables), "ctx": torch.from_numpy(plan.context_lens)}
+    stg = StagedInputs({n: (tuple(x.shape), x.dtype) for n, x in src.items()}, cuda_device)
+    assert all(stg.dev[n].data_ptr() % 256 == 0 for n in src)
+    for n, x in src.items():
+        stg.host[n].copy_(x)
+    stg.upload()
+    torch.cuda.synchronize()
+    for n, x in src.items():
+        assert torch.equal(stg.dev[n].cpu(), x.cpu())
+    d = stg.dev
+    step = type(c.dev)(d["slots"], c.dev.pairs, d["tables"], d["ctx"], c.dev.max_context_len)
+    out = eng.attend(d["q"], step)
+    pkv.check()
+    assert torch.equal(out, c.out)
+
+
+def test_graph_step_replays_the_step(cuda_device):
+    """The staged upload, decode calls and read-back captured in one CUDA graph:
+    replays with new host inputs give the same output as direct calls."""
+    from paged_kv_cache_139_gb300.engine import GraphStep, StagedInputs
+    w = _custom(H=8, Hkv=2, ctx=(5, 300, 1000, 77), S=4)
+    c = Case(w, cuda_device)
+    plan, eng = c.plan, c.eng
+    src = {"q": c.query, "key": c.key, "value": c.value, "slots": torch.from_numpy(plan.slots),
+           "tables": torch.from_numpy(plan.tables), "ctx": torch.from_numpy(plan.context_lens)}
+    stg = StagedInputs({n: (tuple(x.shape), x.dtype) for n, x in src.items()}, cuda_device)
+    for n, x in src.items():
+        stg.host[n].copy_(x)
+    d = stg.dev
+    step = type(c.dev)(d["slots"], c.dev.pairs, d["tables"], d["ctx"], c.dev.max_context_len)
+    out = torch.empty_like(c.out)
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    g = GraphStep(stg, lambda st: eng.prepare(d["q"], d["key"], d["value"], step, out, stream=st), out, h_out)
+    for rep in range(3):
+        q2 = workloads.normal(tuple(c.query.shape), w.dtype, 900 + rep)
+        stg.host["q"].copy_(q2)
+        g.replay()
+        torch.cuda.synchronize()
+        pkv.check()
+        want = eng.attend(q2.to(cuda_device), c.dev)
+        pkv.check()
+        assert torch.equal(h_out.to(cuda_device), want)
