@@ -15,12 +15,9 @@ from paged_kv_cache_139_gb300.engine import PagedKVCache
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("width,B,dtype", [(4, 16, "f16"), (6, 4, "bf16"), (2, 32, "f16")])
-def test_beam_search_steps(cuda_device, width, B, dtype):
-    rng = np.random.default_rng(width * 100 + B)
-    H, Hkv, d = 8, 4, 128
-    prompts = [37, 5, 130]
-    steps = 24
+def _beam_search(cuda_device, width, B, dtype, H, Hkv, prompts, steps, seed):
+    rng = np.random.default_rng(seed)
+    d = 128
     NB = sum(width * (-(-(p + steps + 1) // B)) for p in prompts) + 16
     mb = -(-(max(prompts) + steps + 1) // B)
     order = workloads.free_order(NB, 31 + B)
@@ -32,6 +29,7 @@ def test_beam_search_steps(cuda_device, width, B, dtype):
     beams = [[eng.new_sequence(p)] for p in prompts]
     rbeams = [[ref.seq_new(p)] for p in prompts]
     nq = len(prompts) * width
+    q = None
     for step in range(steps):
         plans = []
         for r in range(len(prompts)):
@@ -67,3 +65,15 @@ def test_beam_search_steps(cuda_device, width, B, dtype):
     used = eng.alloc.blocks_in_use()
     unshared = sum(-(-eng.alloc.seq_len(int(b)) // B) for b in seqs)
     assert used < unshared
+
+
+@pytest.mark.parametrize("width,B,dtype", [(4, 16, "f16"), (6, 4, "bf16"), (2, 32, "f16")])
+def test_beam_search_steps(cuda_device, width, B, dtype):
+    _beam_search(cuda_device, width, B, dtype, 8, 4, [37, 5, 130], 24, width * 100 + B)
+
+
+def test_beam_search_bench_shapes(cuda_device):
+    """The benchmark's beam workload shapes (OPT-13B layer, 40 x 128 MHA, f16, B=16, width 4,
+    16 requests with its lognormal prompts), 32 steps."""
+    w = workloads.beam(width=4)
+    _beam_search(cuda_device, 4, 16, "f16", 40, 40, [int(p) for p in w.context_lens], 32, 7)

@@ -162,3 +162,14 @@ def test_bad_block_is_latched(cuda_device):
         pkv.check()
     assert e.value.status == 3
     assert torch.equal(c.rerun(), c.out)
+
+
+def test_max_query_len_bounds_the_rows(cuda_device):
+    """max_query_len sizes the grid: rows of a sequence past the tiles it
+    covers (256 rows per CTA) are left untouched, the rest are computed."""
+    w = custom((300,), (300,), H=2, Hkv=2)
+    c = PrefillCase(w, cuda_device)
+    o = torch.full_like(c.q_dev, 5.0)
+    c.rerun(out=o, max_query_len=100)
+    assert torch.equal(o[:256], c.out[:256])
+    assert (o[256:] == 5.0).all()

@@ -113,3 +113,32 @@ def test_swap_between_device_pools(cuda_device):
     want = oracle.bits16(torch.zeros_like(b))
     oracle.copy_blocks_between(want, oracle.bits16(a), pairs.cpu().numpy())
     assert np.array_equal(oracle.bits16(b), want)
+
+
+def test_swap_bench_workload(cuda_device):
+    """The benchmark's swap workload (32 Llama-2-7B-layer sequences, 1.1 GB of K+V) swapped out and
+    back through the engine: the host pool holds the oracle's copies, and the GPU pool after the
+    round trip holds every sequence's blocks unchanged."""
+    w = workloads.swap()
+    t = workloads.tensors(w, device=cuda_device)
+    eng = PagedKVCache(w.num_blocks, w.num_kv_heads, w.head_dim, w.block_size, w.torch_dtype, cuda_device,
+                       w.max_blocks_per_seq, workloads.free_order(w.num_blocks, w.seed),
+                       key_cache=t["key_cache"], value_cache=t["value_cache"])
+    host = HostKVPool(w.num_blocks, w.num_kv_heads, w.head_dim, w.block_size, w.torch_dtype)
+    ids = [eng.new_sequence(int(c)) for c in w.context_lens]
+    tables0 = [eng.alloc.block_table(s) for s in ids]
+    gk, gv = oracle.bits16(eng.key_cache), oracle.bits16(eng.value_cache)
+    hids, out_pairs = eng.swap_out(ids, host)
+    pkv.check()
+    want_k = np.zeros_like(gk)
+    oracle.copy_blocks_between(want_k, gk, out_pairs)
+    hk = oracle.bits16(host.key_cache)
+    assert np.array_equal(hk[out_pairs[:, 1]], want_k[out_pairs[:, 1]])
+    eng.key_cache.zero_()
+    eng.value_cache.zero_()
+    gids, in_pairs = eng.swap_in(hids, host)
+    pkv.check()
+    nk, nv = oracle.bits16(eng.key_cache), oracle.bits16(eng.value_cache)
+    for s0, s1 in zip(ids, gids):
+        t0, t1 = tables0[ids.index(s0)], eng.alloc.block_table(s1)
+        assert np.array_equal(nk[t1], gk[t0]) and np.array_equal(nv[t1], gv[t0])
