@@ -374,10 +374,9 @@ def run_ours(args, rank: int, world: int):
         # the host enqueues the step, so no host latency lands between the events
         flush.zero_()
         starts[i].record(stream)
-        prep.copy()
-        prep.write()
+        prep.front()
         mids[i].record(stream)
-        prep.attend()
+        prep.back()
         ends[i].record(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
@@ -471,7 +470,9 @@ def run_ours(args, rank: int, world: int):
         "pct_of_hbm_peak": 100.0 * value / world / peak,
         "tokens_per_s": w.num_seqs * world / (t_step_max * 1e-3),
         "roofline": {"bound": "hbm", "achieved": attn_gbs, "peak": peak, "unit": "GB/s", "frac": attn_gbs / peak,
-                     "traffic": traffic, "kernel": "paged_attention_decode (partition kernel + merge)",
+                     "traffic": traffic, "kernel": ("paged_attention_decode_write (new tokens written in the launch, "
+                                                    "partition kernel + merge)" if prep._fused else
+                                                    "paged_attention_decode (partition kernel + merge)"),
                      "peak_source": f"{peak_src} {'MEASURED_PEAKS.json hbm_gbs' if peak_src == 'measured' else '6.8 TB/s'}",
                      "ms_per_launch": t_attn},
         "paged_overhead": {"contiguous_ms": t_contig, "paged_ms": t_attn,

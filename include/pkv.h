@@ -127,6 +127,36 @@ pkv_status paged_attention_decode(void *out_dev, const void *query_dev,
                                   struct CUstream_st *stream);
 
 /* ---------------------------------------------------------------------------
+ * paged_attention_decode_write -- kv_reshape_and_cache and
+ * paged_attention_decode of one decode step in one launch ("vLLM &
+ * PagedAttention" §X: the fused reshape-and-block-write beside the
+ * attention).  The pages have no single call for the pair; it saves the
+ * write's launch.
+ *
+ * key_dev, value_dev [num_seqs][num_kv_heads][head_dim] hold each sequence's
+ * new token, slot_mapping_dev[num_seqs] (int64) its slot, which must be the
+ * slot of position context_lens[s] - 1 of sequence s's table (as the
+ * allocator returns it); a negative slot writes nothing; a slot beyond the
+ * pool latches PKV_EINDEX.  The result is that of kv_reshape_and_cache on
+ * the same arguments followed by paged_attention_decode: the caches hold the
+ * new tokens bit for bit and out is the attention over contexts that include
+ * them.  When the batch takes the grid kernel (more than 4096 sequences) the
+ * call launches the write first.  Other arguments as for
+ * paged_attention_decode.
+ * ------------------------------------------------------------------------- */
+pkv_status paged_attention_decode_write(void *out_dev, const void *query_dev, const void *key_dev,
+                                        const void *value_dev, void *key_cache_dev,
+                                        void *value_cache_dev, const int64_t *slot_mapping_dev,
+                                        const int32_t *block_tables_dev,
+                                        const int32_t *context_lens_dev, int num_seqs,
+                                        int max_blocks_per_seq, int max_context_len,
+                                        int block_size, int num_blocks, int num_heads,
+                                        int num_kv_heads, int head_dim, float scale,
+                                        int partition_size, void *workspace_dev,
+                                        size_t workspace_bytes, pkv_dtype dtype,
+                                        struct CUstream_st *stream);
+
+/* ---------------------------------------------------------------------------
  * paged_attention_decode_noalloc -- paged_attention_decode for callers that
  * cannot allocate device memory.  The pages have no counterpart: this is an
  * interface convenience of this library.

@@ -24,7 +24,7 @@ import torch
 from ._lib import STATUS, load
 
 __all__ = ["PkvError", "PkvOOM", "kv_reshape_and_cache", "paged_attention_decode",
-           "paged_attention_decode_noalloc", "paged_attention_prefill", "paged_attention_workspace_size",
+           "paged_attention_decode_noalloc", "paged_attention_decode_write", "paged_attention_prefill", "paged_attention_workspace_size",
            "make_workspace",
            "paged_attention_partition_size", "copy_blocks",
            "validate_copy_pairs", "swap_blocks", "check", "launch_count", "version", "BlockAllocator", "library_path"]
@@ -177,6 +177,40 @@ def paged_attention_decode(out: torch.Tensor, query: torch.Tensor, key_cache: to
         S, mb, max_context_len, B, NB, H, Hkv, d, float(scale), partition_size, ws_ptr, ws_bytes,
         _dtype_code(query), _stream(stream, query.device))
     _ck(rc, "paged_attention_decode")
+    return out
+
+
+def paged_attention_decode_write(out: torch.Tensor, query: torch.Tensor, key: torch.Tensor, value: torch.Tensor,
+                                 key_cache: torch.Tensor, value_cache: torch.Tensor, slot_mapping: torch.Tensor,
+                                 block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                 scale: Optional[float] = None, max_context_len: int = 0, partition_size: int = 0,
+                                 workspace: Optional[torch.Tensor] = None,
+                                 stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """kv_reshape_and_cache of each sequence's new token (key/value [S][Hkv][d],
+    slot_mapping int64 [S], the slot of position context_lens[s] - 1) and
+    paged_attention_decode in one launch.  Returns out."""
+    S, H, d = query.shape
+    NB, Hkv, B, d2 = key_cache.shape
+    if d2 != d or out.shape != query.shape or value_cache.shape != key_cache.shape:
+        raise ValueError("paged_attention_decode_write: shape mismatch")
+    if key.shape != (S, Hkv, d) or value.shape != key.shape or slot_mapping.shape != (S,):
+        raise ValueError("paged_attention_decode_write: key/value must be [S][Hkv][d], slot_mapping [S]")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise ValueError("paged_attention_decode_write: block_tables must be [S][max_blocks], context_lens [S]")
+    mb = block_tables.shape[1]
+    mcl = max_context_len if max_context_len > 0 else mb * B
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if workspace is None:
+        workspace = _workspace(query.device, paged_attention_workspace_size(S, H, Hkv, d, mcl, partition_size))
+    rc = load().paged_attention_decode_write(
+        _dev(out, "out"), _dev(query, "query"), _dev(key, "key"), _dev(value, "value"),
+        _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
+        _dev(slot_mapping, "slot_mapping", torch.int64), _dev(block_tables, "block_tables", torch.int32),
+        _dev(context_lens, "context_lens", torch.int32), S, mb, max_context_len, B, NB, H, Hkv, d, float(scale),
+        partition_size, _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _dtype_code(query), _stream(stream, query.device))
+    _ck(rc, "paged_attention_decode_write")
     return out
 
 

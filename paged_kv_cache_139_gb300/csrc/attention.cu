@@ -401,6 +401,10 @@ struct AttnArgs {
     float scale_log2;            // scale * log2(e)
     unsigned int *cnt;           // [S][H] partitions finished (fused merge); zero between calls
     int fused_merge;             // 1: the last partition of a (sequence, head tile) merges them all
+    // the step's new tokens, written into the cache by the kernel (null: already written)
+    const void *new_k;           // [S][Hkv][D]
+    const void *new_v;
+    const int64_t *slots;        // [S]
 };
 
 // splits of up to this many partitions merge inside the attention kernel;
@@ -878,6 +882,31 @@ __global__ void __launch_bounds__(PConf<D, G, MMA>::THREADS, PConf<D, G, MMA>::C
             // have been consumed.
             const int qb = items % NQ;
             int win = cur.win, ent = cur.ent;
+            if (a.new_k && part == nparts - 1) {
+                // The step's new token of sequence s (position ctx - 1, in this partition): the
+                // producer writes its key and value rows for kv head g into the cache, then makes
+                // the writes visible to the copies below (every item that reads the slot writes it
+                // first; items of other kv heads or partitions never read it).
+                constexpr int VEC = D * (int)sizeof(T) / 16;       // 16-byte vectors per row
+                const long long slot = a.slots[s];
+                if (slot >= 0) {
+                    const long long blk = slot >> a.log2_block;
+                    if (blk >= a.num_blocks) {
+                        if (lane == 0) latch(a.st, kFlagBadSlot, slot);
+                    } else if (lane < 2 * VEC) {
+                        const int off = (int)(slot & (B - 1));
+                        const int v = lane % VEC;
+                        const bool isv = lane >= VEC;
+                        const uint4 *src = reinterpret_cast<const uint4 *>(isv ? a.new_v : a.new_k) +
+                                           ((size_t)s * a.num_kv_heads + g) * VEC + v;
+                        uint4 *dst = reinterpret_cast<uint4 *>(const_cast<void *>(isv ? a.v_cache : a.k_cache)) +
+                                     (((size_t)blk * a.num_kv_heads + g) * B + off) * VEC + v;
+                        *dst = __ldg(src);
+                        asm volatile("fence.proxy.async.global;" ::: "memory");
+                    }
+                }
+                __syncwarp();
+            }
             const int i_claim = npad > 2 ? npad - 2 : 0, i_decode = npad > 1 ? npad - 1 : 0;
             for (int i = 0; i < npad; i++, kk++) {
                 if (i == i_claim) {
@@ -1402,13 +1431,17 @@ size_t paged_attention_workspace_size(int num_seqs, int num_heads, int num_kv_he
     return pkv::ws_layout(num_seqs, num_heads, head_dim, pkv::parts_for(max_context_len, P)).bytes;
 }
 
-pkv_status paged_attention_decode(void *out, const void *query, const void *key_cache, const void *value_cache,
-                                  const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
-                                  int max_blocks_per_seq, int max_context_len, int block_size, int num_blocks,
-                                  int num_heads, int num_kv_heads, int head_dim, float scale, int partition_size,
-                                  void *workspace, size_t workspace_bytes, pkv_dtype dtype,
-                                  struct CUstream_st *stream) {
-    using namespace pkv;
+}  // extern "C"
+
+namespace pkv {
+namespace {
+
+pkv_status decode_impl(void *out, const void *query, const void *key_cache, const void *value_cache,
+                       const int32_t *block_tables, const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
+                       int max_context_len, int block_size, int num_blocks, int num_heads, int num_kv_heads,
+                       int head_dim, float scale, int partition_size, void *workspace, size_t workspace_bytes,
+                       pkv_dtype dtype, struct CUstream_st *stream, const void *new_k, const void *new_v,
+                       const int64_t *slots) {
     if (dtype != PKV_F16 && dtype != PKV_BF16) return fail(PKV_EINVAL, "paged_attention_decode: bad dtype %d", (int)dtype);
     if (num_seqs < 0 || num_seqs > 65535 || max_blocks_per_seq < 0 || num_blocks < 0)
         return fail(PKV_EINVAL, "paged_attention_decode: bad sizes (seqs %d, table width %d, blocks %d)", num_seqs,
@@ -1447,7 +1480,19 @@ pkv_status paged_attention_decode(void *out, const void *query, const void *key_
     int G = head_tile(group, true);
     const bool persistent = use_persistent(num_seqs, head_dim, G, 2);
     if (!persistent) G = head_tile(group, false);
+    if (new_k && !persistent) {
+        // the grid kernel has no fused write: write first, then attend
+        const pkv_status ws_ = kv_reshape_and_cache(new_k, new_v, const_cast<void *>(key_cache),
+                                                    const_cast<void *>(value_cache), slots, num_seqs, num_kv_heads,
+                                                    head_dim, block_size, num_blocks, dtype, stream);
+        if (ws_ != PKV_OK) return ws_;
+        new_k = new_v = nullptr;
+        slots = nullptr;
+    }
     AttnArgs a;
+    a.new_k = new_k;
+    a.new_v = new_v;
+    a.slots = slots;
     a.out = out;
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     a.hdr = reinterpret_cast<WsHeader *>(ws);
@@ -1485,6 +1530,40 @@ pkv_status paged_attention_decode(void *out, const void *query, const void *key_
         if (e != cudaSuccess) return fail(PKV_ECUDA, "paged_attention_decode: reduce launch: %s", cudaGetErrorString(e));
     }
     return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" {
+
+pkv_status paged_attention_decode(void *out, const void *query, const void *key_cache, const void *value_cache,
+                                  const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                                  int max_blocks_per_seq, int max_context_len, int block_size, int num_blocks,
+                                  int num_heads, int num_kv_heads, int head_dim, float scale, int partition_size,
+                                  void *workspace, size_t workspace_bytes, pkv_dtype dtype,
+                                  struct CUstream_st *stream) {
+    return pkv::decode_impl(out, query, key_cache, value_cache, block_tables, context_lens, num_seqs,
+                            max_blocks_per_seq, max_context_len, block_size, num_blocks, num_heads, num_kv_heads,
+                            head_dim, scale, partition_size, workspace, workspace_bytes, dtype, stream, nullptr,
+                            nullptr, nullptr);
+}
+
+pkv_status paged_attention_decode_write(void *out, const void *query, const void *key, const void *value,
+                                        void *key_cache, void *value_cache, const int64_t *slot_mapping,
+                                        const int32_t *block_tables, const int32_t *context_lens, int num_seqs,
+                                        int max_blocks_per_seq, int max_context_len, int block_size, int num_blocks,
+                                        int num_heads, int num_kv_heads, int head_dim, float scale,
+                                        int partition_size, void *workspace, size_t workspace_bytes, pkv_dtype dtype,
+                                        struct CUstream_st *stream) {
+    using namespace pkv;
+    if (num_seqs > 0 && (!key || !value || !slot_mapping))
+        return fail(PKV_EINVAL, "paged_attention_decode_write: NULL key, value or slot_mapping");
+    if (num_seqs > 0 && (!aligned16(key) || !aligned16(value)))
+        return fail(PKV_EINVAL, "paged_attention_decode_write: key and value must be 16-byte aligned");
+    return decode_impl(out, query, key_cache, value_cache, block_tables, context_lens, num_seqs, max_blocks_per_seq,
+                       max_context_len, block_size, num_blocks, num_heads, num_kv_heads, head_dim, scale,
+                       partition_size, workspace, workspace_bytes, dtype, stream, key, value, slot_mapping);
 }
 
 }  // extern "C"

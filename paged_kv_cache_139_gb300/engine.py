@@ -306,10 +306,12 @@ class PagedKVCache:
 
     def prepare(self, query: torch.Tensor, key: torch.Tensor, value: torch.Tensor, step: DeviceStep,
                 out: torch.Tensor, scale: Optional[float] = None, partition_size: int = 0,
-                stream: Optional[torch.cuda.Stream] = None) -> "PreparedStep":
+                stream: Optional[torch.cuda.Stream] = None, fused: bool = True) -> "PreparedStep":
         """The device calls of a decode step on fixed buffers, with their C-ABI
-        arguments built once."""
-        return PreparedStep(self, query, key, value, step, out, scale, partition_size, stream)
+        arguments built once.  fused: the cache write rides in the attention
+        launch (paged_attention_decode_write) when the step has one new token
+        per sequence."""
+        return PreparedStep(self, query, key, value, step, out, scale, partition_size, stream, fused)
 
 
 class PreparedStep:
@@ -318,7 +320,8 @@ class PreparedStep:
     step then costs three or four plain C calls.  For decode loops that run
     the same buffers every iteration (the buffers' contents may change)."""
 
-    def __init__(self, eng: PagedKVCache, query, key, value, step: DeviceStep, out, scale, partition_size, stream):
+    def __init__(self, eng: PagedKVCache, query, key, value, step: DeviceStep, out, scale, partition_size, stream,
+                 fused=True):
         self._L = load()
         S, H, d = query.shape
         assert out.shape == query.shape and out.dtype == query.dtype == eng.key_cache.dtype
@@ -342,6 +345,14 @@ class PreparedStep:
                         step.max_context_len, B, NB, H, eng.num_kv_heads, d,
                         float(1.0 / math.sqrt(d) if scale is None else scale), partition_size, ws.data_ptr(),
                         ws.numel(), code, st)
+        # one new token per sequence, in sequence order: the write can ride in the attention launch
+        self._fused = fused and T == S
+        self._write_attend = (out.data_ptr(), query.data_ptr(), key.data_ptr(), value.data_ptr(),
+                              eng.key_cache.data_ptr(), eng.value_cache.data_ptr(), step.slots.data_ptr(),
+                              step.tables.data_ptr(), step.context_lens.data_ptr(), S, step.tables.shape[1],
+                              step.max_context_len, B, NB, H, eng.num_kv_heads, d,
+                              float(1.0 / math.sqrt(d) if scale is None else scale), partition_size, ws.data_ptr(),
+                              ws.numel(), code, st)
 
     def copy(self) -> None:
         for args in self._copy:
@@ -360,10 +371,28 @@ class PreparedStep:
         if rc:
             raise PkvError(rc, "paged_attention_decode")
 
-    def __call__(self) -> None:
+    def write_attend(self) -> None:
+        """The cache write and the attention in one launch (paged_attention_decode_write)."""
+        rc = self._L.paged_attention_decode_write(*self._write_attend)
+        if rc:
+            raise PkvError(rc, "paged_attention_decode_write")
+
+    def front(self) -> None:
+        """What runs before the attention launch: the copies (and the write when not fused)."""
         self.copy()
-        self.write()
-        self.attend()
+        if not self._fused:
+            self.write()
+
+    def back(self) -> None:
+        """The attention launch (with the write when fused)."""
+        if self._fused:
+            self.write_attend()
+        else:
+            self.attend()
+
+    def __call__(self) -> None:
+        self.front()
+        self.back()
 
 
 class PreparedPrefill:

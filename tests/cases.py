@@ -61,7 +61,8 @@ class Case:
     oracle side on demand (oracle_out)."""
 
     def __init__(self, w: workloads.Workload, device="cuda", gen_device="cpu",
-                 subset: Optional[list] = None, partition_size: Optional[int] = None):
+                 subset: Optional[list] = None, partition_size: Optional[int] = None, fused: bool = False):
+        self.fused = fused
         self.w = w
         self.device = torch.device(device)
         self.partition_size = w.partition_size if partition_size is None else partition_size
@@ -141,7 +142,15 @@ class Case:
         self.dev = eng.upload(self.plan)
         self.q_dev = self.query.to(d)
         self.k_dev, self.v_dev = self.key.to(d), self.value.to(d)
-        self.out = eng.decode(self.q_dev, self.k_dev, self.v_dev, self.dev, partition_size=self.partition_size)
+        if self.fused:
+            # the new tokens' write inside the attention launch (paged_attention_decode_write)
+            self.out = torch.empty_like(self.q_dev)
+            prep = eng.prepare(self.q_dev, self.k_dev, self.v_dev, self.dev, self.out,
+                               partition_size=self.partition_size, fused=True)
+            assert prep._fused
+            prep()
+        else:
+            self.out = eng.decode(self.q_dev, self.k_dev, self.v_dev, self.dev, partition_size=self.partition_size)
         self.eng = eng
         pkv.check()                     # raises (and clears) any error the device latched
 

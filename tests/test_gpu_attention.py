@@ -263,12 +263,21 @@ def test_prepared_step_matches_decode(cuda_device):
     w = _custom(H=8, Hkv=4, ctx=(300, 1, 1200), S=3)
     c = Case(w, cuda_device, partition_size=256)
     out = torch.empty_like(c.q_dev)
+    # the write rides in the attention launch (one launch, the merge fused too) ...
     prep = c.eng.prepare(c.q_dev, c.k_dev, c.v_dev, c.dev, out, partition_size=256)
     before = pkv.launch_count()
     prep()
     pkv.check()
-    assert pkv.launch_count() - before == 2
+    assert pkv.launch_count() - before == 1
     assert torch.equal(out, c.out)
+    # ... or takes its own launch
+    out2 = torch.empty_like(c.q_dev)
+    prep2 = c.eng.prepare(c.q_dev, c.k_dev, c.v_dev, c.dev, out2, partition_size=256, fused=False)
+    before = pkv.launch_count()
+    prep2()
+    pkv.check()
+    assert pkv.launch_count() - before == 2
+    assert torch.equal(out2, c.out)
 
 
 def test_staged_inputs_single_upload(cuda_device):
@@ -321,3 +330,40 @@ def test_graph_step_replays_the_step(cuda_device):
         want = eng.attend(q2.to(cuda_device), c.dev)
         pkv.check()
         assert torch.equal(h_out.to(cuda_device), want)
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("tiny", {}), ("opt13b", {}), ("longgqa", dict(num_seqs=2, ctx_len=3000)),
+    ("sampling", dict(num_prompts=4, max_suffix=40)),
+    ("gqa8", dict(H=16, Hkv=2)), ("gqa4_bf16", dict(H=8, Hkv=2, dtype="bf16")), ("b4_d64", dict(B=4, d=64)),
+    ("b128", dict(B=128)),
+])
+def test_fused_write_matches_separate_calls(cuda_device, name, kw):
+    """paged_attention_decode_write (the new tokens written inside the attention
+    launch) leaves the caches bit-identical to kv_reshape_and_cache followed by
+    paged_attention_decode, gives the same output bit for bit, and matches the
+    oracle."""
+    if name in ("tiny", "opt13b", "longgqa", "sampling"):
+        w = workloads.by_name(name, **kw)
+    else:
+        base = dict(ctx=(1, 17, 200, 513, 1030), S=5)
+        base.update(kw)
+        w = _custom(**base)
+    sep = Case(w, cuda_device)
+    fus = Case(w, cuda_device, fused=True)
+    assert torch.equal(sep.eng.key_cache, fus.eng.key_cache) and torch.equal(sep.eng.value_cache, fus.eng.value_cache)
+    assert torch.equal(sep.out, fus.out)
+    _check(fus, what=f"fused {name}")
+
+
+def test_fused_write_bad_slot_latches_eindex(cuda_device):
+    w = _custom(H=4, Hkv=2, ctx=(5, 40, 300), S=3)
+    c = Case(w, cuda_device)
+    slots = c.dev.slots.clone()
+    slots[1] = w.num_blocks * w.block_size + 3
+    out = torch.empty_like(c.q_dev)
+    pkv.paged_attention_decode_write(out, c.q_dev, c.k_dev, c.v_dev, c.eng.key_cache, c.eng.value_cache, slots,
+                                     c.dev.tables, c.dev.context_lens)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.check()
+    assert e.value.status == 3
