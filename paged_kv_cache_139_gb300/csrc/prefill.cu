@@ -93,6 +93,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// max(a, b, c) in one instruction (three-input form, sm_100 and later).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float m;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
+    return m;
+}
+
 __device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity, long long limit) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, limit));
 }
@@ -341,7 +348,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int c = 0; c < 4; c++)
 #pragma unroll
-                            for (int i = 0; i < 32; i++) mxs[i & 3] = fmaxf(mxs[i & 3], __uint_as_float(sr[c][i]));
+                            for (int i = 0; i < 32; i += 2)
+                                mxs[(i >> 1) & 3] = max3(mxs[(i >> 1) & 3], __uint_as_float(sr[c][i]),
+                                                         __uint_as_float(sr[c][i + 1]));
                     } else {
 #pragma unroll
                         for (int c = 0; c < 4; c++)
@@ -350,6 +359,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 if (32 * c + i <= lim) mxs[i & 3] = fmaxf(mxs[i & 3], __uint_as_float(sr[c][i]));
                     }
                 }
+                // pass 2 reads the scores again chunk by chunk, each load in flight while the
+                // previous chunk is computed; the first one already now
+                uint32_t sb[2][32];
+                tc::tmem_ld32(tS, sb[0]);
                 const float mraw = fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3]));
                 const float mx = mraw * c2;                   // -inf when no key of the tile is visible
                 const bool moved = mx > m_run + kRescaleLog2;
@@ -383,38 +396,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     fence_proxy_async_smem();                // generic writes -> tensor-core reads
                 }
-                // pass 2, probabilities written over the scores: two halves, two loads each
+                // pass 2, probabilities written over the scores
                 const float neg_m = -m_run;
                 float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int hf = 0; hf < 2; hf++) {
-                    uint32_t sr[2][32];
+                for (int c = 0; c < 4; c++) {
+                    uint32_t (&sc)[32] = sb[c & 1];
+                    tc::tmem_wait_ld(sc);
+                    if (c < 3) tc::tmem_ld32(tS + 32 * (c + 1), sb[(c + 1) & 1]);
+                    const int kc = 32 * c;
+                    uint32_t pk[kBf16 ? 32 : 16];
 #pragma unroll
-                    for (int c = 0; c < 2; c++) tc::tmem_ld32(tS + 64 * hf + 32 * c, sr[c]);
-#pragma unroll
-                    for (int c = 0; c < 2; c++) tc::tmem_wait_ld(sr[c]);
-#pragma unroll
-                    for (int c = 0; c < 2; c++) {
-                        const int kc = 32 * (2 * hf + c);
-                        uint32_t pk[32];
-#pragma unroll
-                        for (int i = 0; i < 32; i += 2) {
-                            float p0 = fast_exp2(fmaf(__uint_as_float(sr[c][i]), c2, neg_m));
-                            float p1 = fast_exp2(fmaf(__uint_as_float(sr[c][i + 1]), c2, neg_m));
-                            if (!full) {
-                                p0 = kc + i <= lim ? p0 : 0.f;
-                                p1 = kc + i + 1 <= lim ? p1 : 0.f;
-                            }
-                            ls[(i >> 1) & 3] += p0 + p1;
-                            const uint32_t hi = pack16<T>(p0, p1);
-                            pk[i / 2] = hi;
-                            // remainder after rounding (bf16 widens exactly by a shift)
-                            pk[16 + i / 2] = kBf16 ? pack16<T>(p0 - __uint_as_float(hi << 16),
-                                                               p1 - __uint_as_float(hi & 0xffff0000u))
-                                                   : 0u;
+                    for (int i = 0; i < 32; i += 2) {
+                        float p0 = fast_exp2(fmaf(__uint_as_float(sc[i]), c2, neg_m));
+                        float p1 = fast_exp2(fmaf(__uint_as_float(sc[i + 1]), c2, neg_m));
+                        if (!full) {
+                            p0 = kc + i <= lim ? p0 : 0.f;
+                            p1 = kc + i + 1 <= lim ? p1 : 0.f;
                         }
-                        tc::tmem_st32(tS + 64 * hf + 32 * c, pk);
+                        ls[(i >> 1) & 3] += p0 + p1;
+                        const uint32_t hi = pack16<T>(p0, p1);
+                        pk[i / 2] = hi;
+                        // remainder after rounding (bf16 widens exactly by a shift)
+                        if constexpr (kBf16)
+                            pk[16 + i / 2] = pack16<T>(p0 - __uint_as_float(hi << 16),
+                                                       p1 - __uint_as_float(hi & 0xffff0000u));
                     }
+                    if constexpr (kBf16) tc::tmem_st32(tS + kc, pk);
+                    else tc::tmem_st16(tS + kc, pk);
                 }
                 l_run = l_run * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
                 tc::tmem_wait_st();
