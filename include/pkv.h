@@ -218,10 +218,22 @@ pkv_status paged_attention_decode_noalloc(void *out_dev, const void *query_dev,
  *                       sizes the grid, so a larger n_s leaves rows unwritten.
  *   num_blocks          table entries outside [0, num_blocks) latch
  *                       PKV_EINDEX (the call reads block 0 instead).
- * No workspace: the call allocates nothing.  num_seqs <= 65535; head_dim in
- * {64, 128}; block_size a power of two in [4, 128]; num_heads % num_kv_heads
- * == 0; scale > 0 (usually 1/sqrt(head_dim)).  Asynchronous on `stream`; PKV_EINVAL for bad arguments, launching
- * nothing.
+ *   workspace_dev       NULL, or at least 256 bytes prepared once by
+ *                       paged_attention_workspace_init (a decode workspace
+ *                       serves as well).  The work -- pairs of 128-row query
+ *                       tiles of one (sequence, head) -- is spread over one
+ *                       CTA per SM; with a workspace the CTAs take items from
+ *                       a counter in it (balanced), without one each takes a
+ *                       fixed share (round robin).  The call leaves the
+ *                       counter ready for the next; calls sharing a workspace
+ *                       must not overlap on the GPU.  A workspace that was
+ *                       never prepared latches PKV_EINVAL on the device
+ *                       (pkv_check) and computes nothing.
+ * The call allocates nothing.  num_seqs <= 65535; head_dim in {64, 128};
+ * block_size a power of two in [4, 128]; num_heads % num_kv_heads == 0;
+ * scale > 0 (usually 1/sqrt(head_dim)); ceil(max_query_len / 256) x
+ * num_heads x num_seqs <= 2^30.  Asynchronous on `stream`; PKV_EINVAL for
+ * bad arguments, launching nothing.
  * ------------------------------------------------------------------------- */
 pkv_status paged_attention_prefill(void *out_dev, const void *query_dev,
                                    const void *key_cache_dev, const void *value_cache_dev,
@@ -230,7 +242,8 @@ pkv_status paged_attention_prefill(void *out_dev, const void *query_dev,
                                    const int32_t *query_start_dev, int num_seqs, int num_tokens,
                                    int max_query_len, int max_blocks_per_seq, int block_size,
                                    int num_blocks, int num_heads, int num_kv_heads, int head_dim,
-                                   float scale, pkv_dtype dtype, struct CUstream_st *stream);
+                                   float scale, void *workspace_dev, size_t workspace_bytes,
+                                   pkv_dtype dtype, struct CUstream_st *stream);
 
 /* Bytes of workspace paged_attention_decode needs for these sizes: 256 for
  * the counters, plus the partition partials when a context can span more

@@ -218,12 +218,15 @@ def paged_attention_prefill(out: torch.Tensor, query: torch.Tensor, key_cache: t
                             value_cache: torch.Tensor, block_tables: torch.Tensor,
                             context_lens: torch.Tensor, query_start: torch.Tensor,
                             scale: Optional[float] = None, max_query_len: int = 0,
+                            workspace: Optional[torch.Tensor] = None,
                             stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
     """Prompt-phase attention: out/query [T][H][d] hold the new tokens of all
     sequences back to back, query_start int32 [S+1] their offsets; the new
     tokens of sequence s are the last n_s of its context_lens[s] and each
     attends every token up to its own position.  Their keys and values must
-    already be in the cache.  Returns out."""
+    already be in the cache.  workspace: a buffer from make_workspace (its
+    counter balances the work over the SMs); None takes the binding's own.
+    Returns out."""
     T, H, d = query.shape
     NB, Hkv, B, d2 = key_cache.shape
     S = context_lens.shape[0]
@@ -235,11 +238,13 @@ def paged_attention_prefill(out: torch.Tensor, query: torch.Tensor, key_cache: t
         raise TypeError("paged_attention_prefill: dtype mismatch")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
+    ws = _workspace(query.device, 256) if workspace is None else workspace
     rc = load().paged_attention_prefill(
         _dev(out, "out"), _dev(query, "query"), _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
         _dev(block_tables, "block_tables", torch.int32), _dev(context_lens, "context_lens", torch.int32),
         _dev(query_start, "query_start", torch.int32), S, T, max_query_len, block_tables.shape[1], B, NB, H, Hkv,
-        d, float(scale), _dtype_code(query), _stream(stream, query.device))
+        d, float(scale), _dev(ws, "workspace", torch.uint8), ws.numel(), _dtype_code(query),
+        _stream(stream, query.device))
     _ck(rc, "paged_attention_prefill")
     return out
 

@@ -24,7 +24,8 @@ SIGNATURES = {
                                           _i, _p, _sz, _i, _p]),
     "paged_attention_decode_noalloc": (_i, [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i,
                                             _i, _p]),
-    "paged_attention_prefill": (_i, [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _p]),
+    "paged_attention_prefill": (_i, [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f, _p, _sz,
+                                     _i, _p]),
     "paged_attention_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
     "paged_attention_workspace_init": (_i, [_p, _sz, _p]),
     "paged_attention_partition_size": (_i, [_i, _i, _i, _i, _i, _i]),

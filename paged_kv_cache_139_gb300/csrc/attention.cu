@@ -387,7 +387,7 @@ struct AttnArgs {
     const int32_t *tables;       // [S][max_blocks]
     const int32_t *ctx_lens;     // [S]
     DeviceStatus *st;
-    struct WsHeader *hdr;        // work-ticket counters at the head of the workspace
+    WsHeader *hdr;               // work-ticket counters at the head of the workspace
     int num_seqs;
     int max_blocks;
     int max_ctx;
@@ -677,14 +677,6 @@ __global__ void __launch_bounds__(kThreads, min_ctas<G>()) paged_attention_kerne
 // memory and an mbarrier (bounded waits only, no named barriers).
 // ---------------------------------------------------------------------------
 
-struct WsHeader {
-    unsigned int next;        // next ticket
-    unsigned int done;        // CTAs that have taken their last ticket
-    unsigned int magic;       // kWsMagic once paged_attention_workspace_init has run
-    unsigned int pad;
-};
-constexpr unsigned int kWsMagic = 0x31766b70u;
-constexpr size_t kWsHeaderBytes = 256;
 constexpr int kMaxPersistentSeqs = 4096;      // sequence tables kept in shared memory
 constexpr size_t kMaxSmemPerCta = 227 * 1024;
 

@@ -38,6 +38,18 @@ __device__ __forceinline__ void latch(DeviceStatus *st, unsigned int flag, long 
     }
 }
 
+// Head of an attention workspace (paged_attention_workspace_init zeroes the
+// buffer and sets the magic): work-ticket counters of the persistent kernels.
+// A kernel's last CTA leaves the counters at zero for the next call.
+struct WsHeader {
+    unsigned int next;        // next ticket
+    unsigned int done;        // CTAs that have taken their last ticket
+    unsigned int magic;       // kWsMagic once paged_attention_workspace_init has run
+    unsigned int pad;
+};
+constexpr unsigned int kWsMagic = 0x31766b70u;
+constexpr size_t kWsHeaderBytes = 256;
+
 // Cycles a wait on an mbarrier may take before the kernel gives up (about
 // 0.14 s at 1.9 GHz; a stage normally lands within microseconds).
 constexpr long long kWaitLimitCycles = 1ll << 28;

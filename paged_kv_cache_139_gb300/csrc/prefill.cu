@@ -64,13 +64,26 @@ struct PrefillArgs {
     const int32_t *context_lens;
     const int32_t *query_start;
     DeviceStatus *status;
+    WsHeader *hdr;                       // ticket counters; null: static round robin
     int num_seqs, num_tokens, max_blocks, log2_block, num_blocks;
     int num_heads, group;
+    int num_pairs;                       // 256-row tiles pairs per sequence (of the longest)
+    int num_items;                       // num_pairs x num_heads x num_seqs tickets
     float scale_log2;                    // scale * log2(e)
 };
 
-// Shared memory: the two query tiles and the K/V ring.  P stays in TMEM,
-// over the tile's S columns.  The allocation is padded to keep one CTA per
+// A work item as the producer publishes it to the other warps: (sequence s,
+// query head h, the two 128-row tiles from new token t0).
+struct PfItem {
+    int s, h, t0, q_begin, ctx, pos00;   // pos00: position of the item's first new token
+    int rows0, rows1;                    // valid rows of the two tiles (rows1 = 0: one tile)
+    int nkv0, nkv1;                      // key tiles each tile reads
+    int stop;                            // no further items
+    int pad[5];
+};
+
+// Shared memory: the two query tiles, the K/V ring and two item slots.  P
+// stays in TMEM, over the tile's S columns.  The allocation keeps one CTA per
 // SM (each CTA takes all 512 TMEM columns).
 template <int D> struct PfLayout {
     static constexpr int NP = D / 64;                              // panels of d
@@ -78,13 +91,16 @@ template <int D> struct PfLayout {
     static constexpr uint32_t k = q + kTiles * NP * kPanelBytes;    // kStages x NP panels
     static constexpr uint32_t v = k + kStages * NP * kPanelBytes;
     static constexpr uint32_t bars = v + kStages * NP * kPanelBytes;
-    static constexpr uint32_t bytes = bars + 256;
+    static constexpr uint32_t items = bars + 256;
+    static constexpr uint32_t bytes = items + 2 * sizeof(PfItem);
     static constexpr size_t alloc = (bytes + 1024 > 120u * 1024u) ? bytes + 1024 : 120u * 1024u;
 };
 
 // barrier slots
-enum : int { bQFull = 0, bKFull = 1, bVFull = 3, bKEmpty = 5, bVEmpty = 7, bSFull = 9, bPFull = 11, bODone = 13,
-             bDrain = 15, kNumBars = 16 };
+enum : int { bQFull = 0, bQEmpty = 1, bKFull = 2, bVFull = 4, bKEmpty = 6, bVEmpty = 8, bSFull = 10, bPFull = 12,
+             bODone = 14, bItemFull = 16, bItemEmpty = 18, bDrain = 20, kNumBars = 21 };
+// an item slot is released by every softmax warp and the MMA warp
+constexpr int kItemReaders = kTiles * kSoftmaxWarps + 1;
 
 // 2^x by the hardware approximation (MUFU); 2^-inf = 0.
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -127,6 +143,16 @@ template <> __device__ __forceinline__ uint32_t pack16<__nv_bfloat16>(float x, f
 // fp16 (11 bits) needs one.
 __device__ __forceinline__ uint32_t p_col(int t, bool lo) { return 32 * (t >> 1) + 8 * (t & 1) + (lo ? 16 : 0); }
 
+// Ticket t in [0, num_items): the longest pairs of tiles first (pair index
+// descending), then sequence, then head.
+__device__ __forceinline__ void ticket_item(const PrefillArgs &a, int t, int &s, int &h, int &pair) {
+    const int hs = a.num_heads * a.num_seqs;
+    pair = a.num_pairs - 1 - t / hs;
+    const int rem = t % hs;
+    s = rem / a.num_heads;
+    h = rem % a.num_heads;
+}
+
 template <int D, typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_prefill_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmq,
@@ -137,34 +163,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_pf[];
     uint8_t *sm = smem_pf + ((1024u - (smem_u32(smem_pf) & 1023u)) & 1023u);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int pair = (int)gridDim.x - 1 - (int)blockIdx.x;
-    const int h = blockIdx.y, s = blockIdx.z;
+    const int G = (int)gridDim.x;
 
     pdl_wait();
     DeviceStatus *st = a.status;
-    if (timed_out(st)) return;
-    const int q_begin = a.query_start[s], q_end = a.query_start[s + 1], ctx = a.context_lens[s];
-    const int n = q_end - q_begin;
-    const int B = 1 << a.log2_block;
-    const int t0 = pair * kTiles * kRows;
-    if (n < 0 || q_begin < 0 || q_end > a.num_tokens || n > ctx || ctx > a.max_blocks * B) {
-        if (tid == 0 && pair == 0 && h == 0) latch(st, kFlagBadContext, s);
+    WsHeader *hdr = a.hdr;
+    if (hdr && hdr->magic != kWsMagic) {
+        if (blockIdx.x == 0 && tid == 0) latch(st, kFlagBadWorkspace, (long long)hdr->magic);
         return;
     }
-    if (t0 >= n) return;                       // this sequence has fewer tiles
-    // per tile x: valid rows, position of row 0, key tiles read (tile 1 sees at least tile 0's keys)
-    const int rows0 = min(kRows, n - t0), rows1 = max(0, min(kRows, n - t0 - kRows));
-    const int pos00 = ctx - n + t0, pos01 = pos00 + kRows;
-    const int nkv0 = (pos00 + rows0 - 1) / kKeys + 1;
-    const int nkv1 = rows1 ? (pos01 + rows1 - 1) / kKeys + 1 : 0;
-    const int ntiles = rows1 ? 2 : 1;
-    const int nkv = max(nkv0, nkv1);
-    const int g = h / a.group;
+    if (timed_out(st)) {
+        // this CTA claims no ticket, but it still counts towards the counters' reset
+        if (hdr && tid == 0) {
+            __threadfence();
+            if (atomicAdd(&hdr->done, 1u) == (unsigned)G - 1) {
+                hdr->next = 0;
+                hdr->done = 0;
+                __threadfence();
+            }
+        }
+        return;
+    }
+    const int B = 1 << a.log2_block;
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::bars);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + kNumBars);
+    PfItem *items = reinterpret_cast<PfItem *>(sm + L::items);
     if (tid == 0) {
         mbar_init(&bars[bQFull], 1);
+        mbar_init(&bars[bQEmpty], 1);
         for (int i = 0; i < kStages; i++) {
             mbar_init(&bars[bKFull + i], 1);
             mbar_init(&bars[bVFull + i], 1);
@@ -176,6 +203,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars[bPFull + x], kSoftmaxWarps * 32);
             mbar_init(&bars[bODone + x], 1);
         }
+        for (int i = 0; i < 2; i++) {
+            mbar_init(&bars[bItemFull + i], 1);
+            mbar_init(&bars[bItemEmpty + i], kItemReaders);
+        }
         mbar_init(&bars[bDrain], 1);
         fence_mbar_init();
     }
@@ -186,66 +217,143 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tslot;
 
     if (warp == kProducerWarp) {
-        // ---------------- producer: Q tiles once, then K and V per key tile ----------------
+        // ---------------- producer: items, then per item its queries and K/V tiles ----------------
         const uint64_t pol_q = policy_evict_first();
         const uint64_t pol_kv = policy_evict_last();   // read again by the sequence's other tiles and heads
-        bool ok = true;
-        if (lane == 0) {
-            mbar_arrive_expect_tx(&bars[bQFull], ntiles * NP * kPanelBytes);
-            for (int x = 0; x < ntiles; x++)
-                for (int p = 0; p < NP; p++)
-                    tma_load_3d(sm + L::q + (x * NP + p) * kPanelBytes, &tmq, 64 * p, h, q_begin + t0 + x * kRows,
-                                &bars[bQFull], pol_q);
-        }
-        const int32_t *row = a.block_tables + (size_t)s * a.max_blocks;
-        const int nblk_used = (ctx + B - 1) >> a.log2_block;
-        const int bpt = kKeys >> a.log2_block;          // blocks per key tile: 1..32, one per lane
-        auto blocks_in = [&](int jj) { return min(bpt, nblk_used - jj * bpt); };
-        int cur = lane < blocks_in(0) ? row[lane] : 0;  // this lane's block of the current tile
-        int j = 0;
-        for (; j < nkv; j++) {
-            const int stg = j & 1;
-            const int nb = blocks_in(j);
-            // the next tile's block id, read ahead of the waits
-            const int nxt = (j + 1 < nkv && lane < blocks_in(j + 1)) ? row[(j + 1) * bpt + lane] : 0;
-            int phys = cur;
-            if (lane < nb && (phys < 0 || phys >= a.num_blocks)) {
-                latch(st, kFlagBadBlock, phys);
-                phys = 0;                                   // keep the byte count; the output is flagged
-            }
-            const uint32_t bytes = (uint32_t)nb * (uint32_t)B * 128u * NP;
-            for (int which = 0; which < 2; which++) {       // K, then V
-                if (j >= kStages) {
-                    ok = wait_warp(&bars[(which ? bVEmpty : bKEmpty) + stg], ((j >> 1) - 1) & 1, kWaitLimitCycles);
-                    if (!ok) break;
+        // the ticket after `prev` (dynamic: a new claim)
+        auto next_ticket = [&](int prev) -> int {
+            if (!hdr) return prev + G;
+            unsigned t = 0;
+            if (lane == 0) t = (unsigned)G + atomicAdd(&hdr->next, 1u);
+            t = __shfl_sync(0xffffffffu, t, 0);
+            return t > (unsigned)a.num_items ? a.num_items : (int)t;
+        };
+        // the first item with work at or after ticket t (following the claims); stop when none
+        auto resolve = [&](int t, PfItem &o) -> int {
+            while (t < a.num_items) {
+                int s, h, pair;
+                ticket_item(a, t, s, h, pair);
+                const int qb = a.query_start[s], qe = a.query_start[s + 1], ctx = a.context_lens[s];
+                const int n = qe - qb, t0 = pair * kTiles * kRows;
+                if (n < 0 || qb < 0 || qe > a.num_tokens || n > ctx || ctx > a.max_blocks * B) {
+                    if (lane == 0 && pair == 0 && h == 0) latch(st, kFlagBadContext, s);
+                } else if (t0 < n) {
+                    o.s = s;
+                    o.h = h;
+                    o.t0 = t0;
+                    o.q_begin = qb;
+                    o.ctx = ctx;
+                    o.pos00 = ctx - n + t0;
+                    o.rows0 = min(kRows, n - t0);
+                    o.rows1 = max(0, min(kRows, n - t0 - kRows));
+                    o.nkv0 = (o.pos00 + o.rows0 - 1) / kKeys + 1;
+                    o.nkv1 = o.rows1 ? (o.pos00 + kRows + o.rows1 - 1) / kKeys + 1 : 0;
+                    o.stop = 0;
+                    return t;
                 }
-                uint64_t *full = &bars[(which ? bVFull : bKFull) + stg];
-                if (lane == 0) mbar_arrive_expect_tx(full, bytes);
-                __syncwarp();
-                uint8_t *dst = sm + (which ? L::v : L::k) + (uint32_t)stg * NP * kPanelBytes;
-                if (lane < nb)
+                t = next_ticket(t);
+            }
+            o.stop = 1;
+            return t;
+        };
+        bool ok = true;
+        int k = 0;       // items published
+        int gj = 0;      // key tiles loaded: ring position
+        int j = 0;
+        PfItem cur;
+        int cur_t = resolve((int)blockIdx.x, cur);
+        for (;; k++) {
+            const int slot = k & 1;
+            if (k >= 2) {
+                ok = wait_warp(&bars[bItemEmpty + slot], ((k >> 1) - 1) & 1, kWaitLimitCycles);
+                if (!ok) break;
+            }
+            if (lane == 0) items[slot] = cur;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[bItemFull + slot]);
+            if (cur.stop) break;
+            // the previous item's products must have read its queries
+            if (k >= 1) {
+                ok = wait_warp(&bars[bQEmpty], (k - 1) & 1, kWaitLimitCycles);
+                if (!ok) break;
+            }
+            const int ntiles = cur.rows1 ? 2 : 1, nkv = max(cur.nkv0, cur.nkv1);
+            const int g = cur.h / a.group;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bars[bQFull], ntiles * NP * kPanelBytes);
+                for (int x = 0; x < ntiles; x++)
                     for (int p = 0; p < NP; p++)
-                        tma_load_4d(dst + p * kPanelBytes + (uint32_t)lane * B * 128u, which ? &tmv : &tmk, 64 * p, 0,
-                                    g, phys, full, pol_kv);
+                        tma_load_3d(sm + L::q + (x * NP + p) * kPanelBytes, &tmq, 64 * p, cur.h,
+                                    cur.q_begin + cur.t0 + x * kRows, &bars[bQFull], pol_q);
+            }
+            const int32_t *row = a.block_tables + (size_t)cur.s * a.max_blocks;
+            const int nblk_used = (cur.ctx + B - 1) >> a.log2_block;
+            const int bpt = kKeys >> a.log2_block;          // blocks per key tile: 1..32, one per lane
+            auto blocks_in = [&](int jj) { return min(bpt, nblk_used - jj * bpt); };
+            int cb = lane < blocks_in(0) ? row[lane] : 0;  // this lane's block of the current tile
+            PfItem nxt_item;
+            int nxt_t = 0;
+            for (j = 0; j < nkv; j++, gj++) {
+                const int stg = gj & 1;
+                const int nb = blocks_in(j);
+                // the next tile's block id, read ahead of the waits
+                const int nxt = (j + 1 < nkv && lane < blocks_in(j + 1)) ? row[(j + 1) * bpt + lane] : 0;
+                int phys = cb;
+                if (lane < nb && (phys < 0 || phys >= a.num_blocks)) {
+                    latch(st, kFlagBadBlock, phys);
+                    phys = 0;                                   // keep the byte count; the output is flagged
+                }
+                const uint32_t bytes = (uint32_t)nb * (uint32_t)B * 128u * NP;
+                for (int which = 0; which < 2; which++) {       // K, then V
+                    if (gj >= kStages) {
+                        ok = wait_warp(&bars[(which ? bVEmpty : bKEmpty) + stg], ((gj >> 1) - 1) & 1,
+                                       kWaitLimitCycles);
+                        if (!ok) break;
+                    }
+                    uint64_t *full = &bars[(which ? bVFull : bKFull) + stg];
+                    if (lane == 0) mbar_arrive_expect_tx(full, bytes);
+                    __syncwarp();
+                    uint8_t *dst = sm + (which ? L::v : L::k) + (uint32_t)stg * NP * kPanelBytes;
+                    if (lane < nb)
+                        for (int p = 0; p < NP; p++)
+                            tma_load_4d(dst + p * kPanelBytes + (uint32_t)lane * B * 128u, which ? &tmv : &tmk,
+                                        64 * p, 0, g, phys, full, pol_kv);
+                }
+                if (!ok) break;
+                cb = nxt;
+                // claim and look up the next item while this one's tiles stream in
+                if (j == 0) nxt_t = resolve(next_ticket(cur_t), nxt_item);
             }
             if (!ok) break;
-            cur = nxt;
+            cur = nxt_item;
+            cur_t = nxt_t;
         }
         if (!ok) {
-            if (lane == 0) latch(st, kFlagTimeout, j);
+            if (lane == 0) latch(st, kFlagTimeout, gj);
             // copies already issued must land before the CTA's memory is reused
-            for (int jj = max(0, j - kStages); jj < j; jj++) {
+            for (int jj = max(0, gj - kStages); jj <= gj; jj++) {
                 mbar_wait(&bars[bKFull + (jj & 1)], (jj >> 1) & 1, kDrainLimitCycles);
                 mbar_wait(&bars[bVFull + (jj & 1)], (jj >> 1) & 1, kDrainLimitCycles);
             }
-            mbar_wait(&bars[bQFull], 0, kDrainLimitCycles);
+            mbar_wait(&bars[bQFull], k & 1, kDrainLimitCycles);
+        }
+        // the last CTA to finish leaves the counters at zero for the next call
+        if (hdr && lane == 0) {
+            __threadfence();
+            if (atomicAdd(&hdr->done, 1u) == (unsigned)G - 1) {
+                hdr->next = 0;
+                hdr->done = 0;
+                __threadfence();
+            }
         }
     } else if (warp == kMmaWarp) {
         // ---------------- MMA issue (one thread) ----------------
-        // Order: S_0(0) S_1(0), then per key tile j: O_0 += P_0 V_j, S_0(j+1), O_1 += P_1 V_j,
+        // Per item: S_0(0) S_1(0), then per key tile j: O_0 += P_0 V_j, S_0(j+1), O_1 += P_1 V_j,
         // S_1(j+1): while one tile's softmax runs, the tensor core works on the other's products.
         // The products of one thread run in issue order, so S(j+1) overwrites P(j) only after
-        // O += P(j) V_j has read it.
+        // O += P(j) V_j has read it, and the next item's first S only after this item's last
+        // product.  The next item's first O product (which overwrites O) waits for that tile's
+        // first P, which its softmax threads write only after they have read this item's O.
         if (lane == 0) {
             const uint32_t id_s = tc::idesc_f16(kRows, kKeys, kBf16, false);
             // O += P V: one product of N = D per 16 keys (for D = 128 the two 64-wide panels of V
@@ -256,10 +364,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t k_base = smem_u32(sm + L::k) + (uint32_t)stg * NP * kPanelBytes;
                 const uint32_t qx = q_base + (uint32_t)x * NP * kPanelBytes;
 #pragma unroll
-                for (int k = 0; k < D / 16; k++) {
-                    const uint32_t off = (k / 4) * kPanelBytes + (k % 4) * 32;
+                for (int kk = 0; kk < D / 16; kk++) {
+                    const uint32_t off = (kk / 4) * kPanelBytes + (kk % 4) * 32;
                     tc::mma_f16_ss(tmem + x * kTileCols, tc::smem_desc_sw128(qx + off, 1024, 1024),
-                                   tc::smem_desc_sw128(k_base + off, 1024, 1024), id_s, k > 0);
+                                   tc::smem_desc_sw128(k_base + off, 1024, 1024), id_s, kk > 0);
                 }
                 tc::mma_commit(&bars[bSFull + x]);
             };
@@ -274,38 +382,54 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        tc::smem_desc_sw128(v_base + t * 2048, kPanelBytes, 1024), id_o,
                                        (acc || part > 0 || t > 0) ? 1u : 0u);
             };
-            bool ok = mbar_wait(&bars[bQFull], 0, kWaitLimitCycles) && mbar_wait(&bars[bKFull], 0, kWaitLimitCycles);
-            int j = 0;
-            if (ok) {
+            bool ok = true;
+            int gj = 0, pc[kTiles] = {0, 0};
+            int k = 0;
+            for (;; k++) {
+                const int slot = k & 1;
+                ok = mbar_wait(&bars[bItemFull + slot], (k >> 1) & 1, kWaitLimitCycles);
+                if (!ok) break;
+                const PfItem it = items[slot];
+                mbar_arrive(&bars[bItemEmpty + slot]);
+                if (it.stop) break;
+                const int ntiles = it.rows1 ? 2 : 1, nkv = max(it.nkv0, it.nkv1);
+                ok = mbar_wait(&bars[bQFull], k & 1, kWaitLimitCycles) &&
+                     mbar_wait(&bars[bKFull + (gj & 1)], (gj >> 1) & 1, kWaitLimitCycles);
+                if (!ok) break;
                 tc::fence_after();
-                for (int x = 0; x < ntiles; x++) issue_s(x, 0);
-                tc::mma_commit(&bars[bKEmpty]);
-                for (; j < nkv && ok; j++) {
-                    const int stg = j & 1;
-                    ok = mbar_wait(&bars[bVFull + stg], (j >> 1) & 1, kWaitLimitCycles);
+                for (int x = 0; x < ntiles; x++) issue_s(x, gj & 1);
+                tc::mma_commit(&bars[bKEmpty + (gj & 1)]);
+                if (nkv == 1) tc::mma_commit(&bars[bQEmpty]);   // the item's last S has been issued
+                for (int j = 0; j < nkv && ok; j++) {
+                    const int g = gj + j, stg = g & 1;
+                    ok = mbar_wait(&bars[bVFull + stg], (g >> 1) & 1, kWaitLimitCycles);
                     for (int x = 0; x < ntiles && ok; x++) {
-                        const int nkv_x = x ? nkv1 : nkv0;
+                        const int nkv_x = x ? it.nkv1 : it.nkv0;
                         if (j >= nkv_x) continue;
-                        ok = mbar_wait(&bars[bPFull + x], j & 1, kWaitLimitCycles);
+                        ok = mbar_wait(&bars[bPFull + x], pc[x] & 1, kWaitLimitCycles);
+                        pc[x]++;
                         if (!ok) break;
                         tc::fence_after();
                         issue_o(x, stg, j > 0);
                         if (j + 1 == nkv_x) {
                             tc::mma_commit(&bars[bODone + x]);
                         } else {
-                            ok = mbar_wait(&bars[bKFull + ((j + 1) & 1)], ((j + 1) >> 1) & 1, kWaitLimitCycles);
+                            ok = mbar_wait(&bars[bKFull + ((g + 1) & 1)], ((g + 1) >> 1) & 1, kWaitLimitCycles);
                             if (!ok) break;
                             tc::fence_after();
-                            issue_s(x, (j + 1) & 1);
+                            issue_s(x, (g + 1) & 1);
                         }
                     }
                     if (ok) {
-                        tc::mma_commit(&bars[bVEmpty + stg]);               // V_j read by every tile
-                        if (j + 1 < nkv) tc::mma_commit(&bars[bKEmpty + ((j + 1) & 1)]);   // K_{j+1} too
+                        tc::mma_commit(&bars[bVEmpty + stg]);                        // V_j read by every tile
+                        if (j + 1 < nkv) tc::mma_commit(&bars[bKEmpty + ((g + 1) & 1)]);   // K_{j+1} too
+                        if (j + 2 == nkv) tc::mma_commit(&bars[bQEmpty]);            // and the last S issued
                     }
                 }
+                if (!ok) break;
+                gj += nkv;
             }
-            if (!ok) latch(st, kFlagTimeout, 1000000 + j);
+            if (!ok) latch(st, kFlagTimeout, 1000000 + k);
             // every MMA issued so far, and every arrive it makes, completes before the CTA
             // frees its TMEM and shared memory
             tc::mma_commit(&bars[bDrain]);
@@ -319,15 +443,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = (uint32_t)(32 * (warp % 4)) << 16;
         const uint32_t tS = tmem + x * kTileCols + lane_off, tO = tS + kKeys;
         bool ok = true;
-        const int rows_x = x ? rows1 : rows0, pos0_x = x ? pos01 : pos00, nkv_x = x ? nkv1 : nkv0;
-        if (rows_x > 0) {
+        int gj = 0, sc = 0, u = 0, k = 0, j = 0;
+        for (;; k++) {
+            const int slot = k & 1;
+            ok = wait_warp(&bars[bItemFull + slot], (k >> 1) & 1, kWaitLimitCycles);
+            if (!ok) break;
+            const PfItem it = items[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[bItemEmpty + slot]);
+            if (it.stop) break;
+            const int nkv = max(it.nkv0, it.nkv1);
+            const int gbase = gj;
+            gj += nkv;
+            const int rows_x = x ? it.rows1 : it.rows0;
+            if (rows_x <= 0) continue;
+            const int pos0_x = it.pos00 + x * kRows, nkv_x = x ? it.nkv1 : it.nkv0;
             const int my_pos = r < rows_x ? pos0_x + r : pos0_x + rows_x - 1;   // last key this row sees
             float m_run = -INFINITY, l_run = 0.f;
             // the tile that zeroes V rows past the context (before its product reads them)
-            const bool zero_duty = (x == 0) == (nkv0 == nkv);
-            int j = 0;
-            for (; j < nkv_x; j++) {
-                ok = wait_warp(&bars[bSFull + x], j & 1, kWaitLimitCycles);
+            const bool zero_duty = (x == 0) == (it.nkv0 == nkv);
+            for (j = 0; j < nkv_x; j++) {
+                ok = wait_warp(&bars[bSFull + x], sc & 1, kWaitLimitCycles);
+                sc++;
                 if (!ok) break;
                 tc::fence_after();
                 const int lim = my_pos - j * kKeys;          // keys 0..lim of this tile are visible
@@ -382,12 +519,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 const int kbase = j * kKeys;
-                if (zero_duty && j == nkv - 1 && kbase + kKeys > ctx) {
+                if (zero_duty && j == nkv - 1 && kbase + kKeys > it.ctx) {
                     // rows past the end of the context hold other data: P is 0 there, but 0 x NaN is not
-                    ok = wait_warp(&bars[bVFull + (j & 1)], (j >> 1) & 1, kWaitLimitCycles);
+                    const int g = gbase + j;
+                    ok = wait_warp(&bars[bVFull + (g & 1)], (g >> 1) & 1, kWaitLimitCycles);
                     if (!ok) break;
-                    const int first = ctx - kbase;
-                    uint8_t *vs = sm + L::v + (uint32_t)(j & 1) * NP * kPanelBytes;
+                    const int first = it.ctx - kbase;
+                    uint8_t *vs = sm + L::v + (uint32_t)(g & 1) * NP * kPanelBytes;
                     const int nvec = (kKeys - first) * 8;    // 16-byte vectors per panel
                     for (int i = r; i < nvec * NP; i += kSoftmaxWarps * 32) {
                         const int p = i / nvec, rem = i % nvec;
@@ -430,33 +568,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::fence_before();
                 mbar_arrive(&bars[bPFull + x]);
             }
-            if (ok) ok = wait_warp(&bars[bODone + x], 0, kWaitLimitCycles);
-            if (ok) {
-                tc::fence_after();
-                const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-                T *orow = reinterpret_cast<T *>(a.out) +
-                          ((size_t)(q_begin + t0 + x * kRows + r) * a.num_heads + h) * D;
+            if (!ok) break;
+            ok = wait_warp(&bars[bODone + x], u & 1, kWaitLimitCycles);
+            u++;
+            if (!ok) break;
+            tc::fence_after();
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            T *orow = reinterpret_cast<T *>(a.out) + ((size_t)(it.q_begin + it.t0 + x * kRows + r) * a.num_heads + it.h) * D;
 #pragma unroll
-                for (int c = 0; c < D / 32; c++) {
-                    uint32_t o[32];
-                    tc::tmem_ld32(tO + 32 * c, o);
-                    tc::tmem_wait_ld(o);
-                    if (r < rows_x) {
+            for (int c = 0; c < D / 32; c++) {
+                uint32_t o[32];
+                tc::tmem_ld32(tO + 32 * c, o);
+                tc::tmem_wait_ld(o);
+                if (r < rows_x) {
 #pragma unroll
-                        for (int v = 0; v < 4; v++) {
-                            uint4 w;
-                            w.x = pack16<T>(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
-                            w.y = pack16<T>(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
-                            w.z = pack16<T>(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
-                            w.w = pack16<T>(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-                            *reinterpret_cast<uint4 *>(orow + 32 * c + 8 * v) = w;
-                        }
+                    for (int v = 0; v < 4; v++) {
+                        uint4 w;
+                        w.x = pack16<T>(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
+                        w.y = pack16<T>(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
+                        w.z = pack16<T>(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
+                        w.w = pack16<T>(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
+                        *reinterpret_cast<uint4 *>(orow + 32 * c + 8 * v) = w;
                     }
                 }
-            } else if (lane == 0) {
-                latch(st, kFlagTimeout, 2000000 + j);
             }
         }
+        if (!ok && lane == 0) latch(st, kFlagTimeout, 2000000 + 1000 * k + j);
     }
     tc::fence_before();
     __syncthreads();
@@ -494,10 +631,10 @@ cudaError_t launch_prefill(const PrefillArgs &a, const void *query, const void *
     if (!encode_tiled16(&tmq, query, 3, qdims, qstr, qbox, kBf16) || !encode_tiled16(&tmk, kc, 4, cdims, cstr, cbox, kBf16) ||
         !encode_tiled16(&tmv, vc, 4, cdims, cstr, cbox, kBf16))
         return cudaErrorInvalidValue;
-    const int rows_per_cta = kTiles * kRows;
-    const dim3 grid((unsigned)((max_query_len + rows_per_cta - 1) / rows_per_cta), (unsigned)a.num_heads,
-                    (unsigned)a.num_seqs);
-    return launch(kern, grid, dim3(kThreads), L::alloc, stream, a, tmq, tmk, tmv);
+    // persistent CTAs, one per SM (each holds all of its SM's TMEM), at most one per item
+    const int sms = sm_count();
+    const int ctas = a.num_items < sms ? a.num_items : sms;
+    return launch(kern, dim3((unsigned)(ctas > 0 ? ctas : 1)), dim3(kThreads), L::alloc, stream, a, tmq, tmk, tmv);
 }
 
 }  // namespace
@@ -510,7 +647,8 @@ extern "C" pkv_status paged_attention_prefill(void *out, const void *query, cons
                                               const int32_t *context_lens, const int32_t *query_start, int num_seqs,
                                               int num_tokens, int max_query_len, int max_blocks_per_seq,
                                               int block_size, int num_blocks, int num_heads, int num_kv_heads,
-                                              int head_dim, float scale, pkv_dtype dtype, struct CUstream_st *stream) {
+                                              int head_dim, float scale, void *workspace, size_t workspace_bytes,
+                                              pkv_dtype dtype, struct CUstream_st *stream) {
     if (num_seqs < 0 || num_tokens < 0 || max_query_len < 0)
         return fail(PKV_EINVAL, "paged_attention_prefill: negative size (num_seqs %d, num_tokens %d, max_query_len %d)",
                     num_seqs, num_tokens, max_query_len);
@@ -537,6 +675,15 @@ extern "C" pkv_status paged_attention_prefill(void *out, const void *query, cons
         return fail(PKV_EINVAL, "paged_attention_prefill: null pointer");
     if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) || !aligned16(value_cache))
         return fail(PKV_EINVAL, "paged_attention_prefill: out, query and caches must be 16-byte aligned");
+    if (workspace && (!aligned16(workspace) || workspace_bytes < kWsHeaderBytes))
+        return fail(PKV_EINVAL, "paged_attention_prefill: workspace must be 16-byte aligned and at least %zu bytes",
+                    kWsHeaderBytes);
+    const int rows_per_pair = kTiles * kRows;
+    const long long num_pairs = ((long long)max_query_len + rows_per_pair - 1) / rows_per_pair;
+    const long long num_items = num_pairs * num_heads * num_seqs;
+    if (num_items > INT_MAX / 2)
+        return fail(PKV_EINVAL, "paged_attention_prefill: %lld work items (query tile pairs x heads x sequences) "
+                                "above 2^30", num_items);
     DeviceStatus *st = status_ptr();
     if (!st) return fail(PKV_ECUDA, "paged_attention_prefill: no device status word");
     PrefillArgs a;
@@ -545,6 +692,9 @@ extern "C" pkv_status paged_attention_prefill(void *out, const void *query, cons
     a.context_lens = context_lens;
     a.query_start = query_start;
     a.status = st;
+    a.hdr = reinterpret_cast<WsHeader *>(workspace);
+    a.num_pairs = (int)num_pairs;
+    a.num_items = (int)num_items;
     a.num_seqs = num_seqs;
     a.num_tokens = num_tokens;
     a.max_blocks = max_blocks_per_seq;

@@ -259,6 +259,13 @@ class PagedKVCache:
         self.write(key, value, step.slots)
         return self.attend(query, step, out, scale, partition_size)
 
+    def prefill_workspace(self) -> torch.Tensor:
+        """The prompt-phase attention's work counter (256 bytes, prepared
+        once); the cache's prefill calls share it, one at a time."""
+        if getattr(self, "_pf_ws", None) is None:
+            self._pf_ws = make_workspace(self.device, 256)
+        return self._pf_ws
+
     def prefill(self, query: torch.Tensor, key: torch.Tensor, value: torch.Tensor, step: DevicePrefill,
                 out: Optional[torch.Tensor] = None, scale: Optional[float] = None) -> torch.Tensor:
         """The device half of a prompt-phase step: copy-on-write copies (a
@@ -270,7 +277,7 @@ class PagedKVCache:
         self.write(key, value, step.slots)
         return paged_attention_prefill(out, query, self.key_cache, self.value_cache, step.tables,
                                        step.context_lens, step.query_start, scale=scale,
-                                       max_query_len=step.max_query_len)
+                                       max_query_len=step.max_query_len, workspace=self.prefill_workspace())
 
     # -- swapping ----------------------------------------------------------------
     def swap_out(self, seqs: Sequence[int], host: HostKVPool, stream=None):
@@ -408,7 +415,8 @@ class PreparedPrefill:
             assert t.is_cuda and t.is_contiguous()
         code = 1 if query.dtype == torch.bfloat16 else 0
         st = ctypes.c_void_p((stream or torch.cuda.current_stream(eng.device)).cuda_stream)
-        self._keep = (query, key, value, step, out)
+        ws = eng.prefill_workspace()
+        self._keep = (query, key, value, step, out, ws)
         NB, B = eng.num_blocks, eng.block_size
         block_bytes = eng.num_kv_heads * B * d * eng.key_cache.element_size()
         n = step.pairs.shape[0] if step.pairs.dim() == 2 else 0
@@ -421,7 +429,8 @@ class PreparedPrefill:
         self._attend = (out.data_ptr(), query.data_ptr(), eng.key_cache.data_ptr(), eng.value_cache.data_ptr(),
                         step.tables.data_ptr(), step.context_lens.data_ptr(), step.query_start.data_ptr(), S, T,
                         step.max_query_len, step.tables.shape[1], B, NB, H, eng.num_kv_heads, d,
-                        float(1.0 / math.sqrt(d) if scale is None else scale), code, st)
+                        float(1.0 / math.sqrt(d) if scale is None else scale), ws.data_ptr(), ws.numel(), code,
+                        st)
 
     def copy(self) -> None:
         for args in self._copy:

@@ -66,18 +66,19 @@ def test_attention_rejects_bad_arguments(over):
 
 def _call_prefill(**over):
     args = dict(out=16, query=16, kc=16, vc=16, bt=16, cl=16, qs=16, S=2, T=10, mql=0, mb=4, B=16, NB=8, H=4,
-                Hkv=2, d=128, scale=0.1, dt=0, st=None)
+                Hkv=2, d=128, scale=0.1, ws=None, wsb=0, dt=0, st=None)
     args.update(over)
     return _lib.load().paged_attention_prefill(
         args["out"], args["query"], args["kc"], args["vc"], args["bt"], args["cl"], args["qs"], args["S"],
         args["T"], args["mql"], args["mb"], args["B"], args["NB"], args["H"], args["Hkv"], args["d"],
-        args["scale"], args["dt"], args["st"])
+        args["scale"], args["ws"], args["wsb"], args["dt"], args["st"])
 
 
 @pytest.mark.parametrize("over", [
     dict(d=96), dict(d=0), dict(B=12), dict(B=2), dict(B=256), dict(H=5, Hkv=2), dict(Hkv=0), dict(dt=7),
     dict(S=-1), dict(T=-3), dict(mql=-1), dict(S=70000), dict(out=None), dict(qs=None), dict(query=18),
     dict(NB=0), dict(scale=float("inf")), dict(scale=float("nan")), dict(scale=0.0), dict(scale=-0.1),
+    dict(ws=16, wsb=128), dict(ws=24, wsb=256), dict(S=65535, H=65535, Hkv=1, T=1 << 20, mql=1 << 20),
 ])
 def test_prefill_rejects_bad_arguments(over):
     assert _call_prefill(**over) == 1                    # PKV_EINVAL, before any launch

@@ -165,11 +165,98 @@ def test_bad_block_is_latched(cuda_device):
 
 
 def test_max_query_len_bounds_the_rows(cuda_device):
-    """max_query_len sizes the grid: rows of a sequence past the tiles it
-    covers (256 rows per CTA) are left untouched, the rest are computed."""
+    """max_query_len bounds the work items: rows of a sequence past the tile
+    pairs it covers (256 rows each) are left untouched, the rest are computed."""
     w = custom((300,), (300,), H=2, Hkv=2)
     c = PrefillCase(w, cuda_device)
     o = torch.full_like(c.q_dev, 5.0)
     c.rerun(out=o, max_query_len=100)
     assert torch.equal(o[:256], c.out[:256])
     assert (o[256:] == 5.0).all()
+
+
+def _prefill_abi(c: PrefillCase, out, workspace, nbytes):
+    """paged_attention_prefill through the C ABI with an explicit workspace
+    pointer (None: the static share per CTA)."""
+    from paged_kv_cache_139_gb300 import _lib
+    w = c.w
+    rc = _lib.load().paged_attention_prefill(
+        out.data_ptr(), c.q_dev.data_ptr(), c.eng.key_cache.data_ptr(), c.eng.value_cache.data_ptr(),
+        c.dev.tables.data_ptr(), c.dev.context_lens.data_ptr(), c.dev.query_start.data_ptr(), w.num_seqs,
+        c.q_dev.shape[0], c.dev.max_query_len, c.dev.tables.shape[1], w.block_size, w.num_blocks, w.num_heads,
+        w.num_kv_heads, w.head_dim, float(1.0 / np.sqrt(w.head_dim)), workspace, nbytes,
+        1 if w.dtype == "bf16" else 0, torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, _lib.load().pkv_last_error_string()
+
+
+def _many_items(seed, S=16, H=32, Hkv=8, d=64, dtype="bf16"):
+    """Several hundred work items (pairs of 128-row tiles x heads x
+    sequences) over the GPU's SMs: every CTA runs several, of different
+    lengths, one- and two-tile, with the item order mixing sequences."""
+    rng = np.random.default_rng(seed)
+    new = rng.integers(1, 420, size=S)
+    cached = rng.integers(0, 200, size=S)
+    return custom(new + cached, new, H=H, Hkv=Hkv, d=d, dtype=dtype, seed=seed)
+
+
+def _item_rows(c: PrefillCase, seed=0):
+    """(token, head) rows covering every work item: per (sequence, head, pair
+    of tiles) the first and last row of each tile and one between."""
+    rng = np.random.default_rng(seed)
+    which = []
+    for s in range(c.w.num_seqs):
+        a, b = int(c.query_start[s]), int(c.query_start[s + 1])
+        for t0 in range(0, b - a, 256):
+            for h in range(c.w.num_heads):
+                for lo in (t0, t0 + 128):
+                    hi = min(lo + 128, b - a)
+                    if lo >= hi:
+                        continue
+                    which += [(a + lo, h), (a + hi - 1, h), (a + int(rng.integers(lo, hi)), h)]
+    return sorted(set(which))
+
+
+@pytest.mark.parametrize("seed,S,H,Hkv,d,dtype", [(11, 16, 32, 8, 64, "bf16"), (12, 24, 24, 24, 128, "f16"),
+                                                   (13, 12, 48, 8, 128, "bf16")])
+def test_many_items_per_cta(cuda_device, seed, S, H, Hkv, d, dtype):
+    """Rows of every work item of a batch whose items outnumber the CTAs
+    several times, against the oracle (pools bit for bit); the static round
+    robin (no workspace) gives the same bits as the counter."""
+    c = PrefillCase(_many_items(seed, S=S, H=H, Hkv=Hkv, d=d, dtype=dtype), cuda_device)
+    items = sum(-(-int(n) // 256) for n in c.w.query_lens) * H
+    assert items > 3 * torch.cuda.get_device_properties(0).multi_processor_count
+    _check(c, f"many items {seed}", which=_item_rows(c, seed))
+    o = torch.full_like(c.q_dev, 3.0)
+    _prefill_abi(c, o, None, 0)
+    pkv.check()
+    assert torch.equal(o, c.out)
+
+
+def test_workspace_counter_left_ready(cuda_device):
+    """After a call the workspace's ticket counters are back at zero (magic
+    kept), so back-to-back calls and graph replays start from ticket 0."""
+    c = PrefillCase(_many_items(21), cuda_device)
+    ws = pkv.make_workspace(cuda_device, 256)
+    before = ws[:16].clone()
+    for _ in range(3):
+        o = torch.empty_like(c.q_dev)
+        _prefill_abi(c, o, ws.data_ptr(), ws.numel())
+        pkv.check()
+        assert torch.equal(o, c.out)
+    torch.cuda.synchronize()
+    assert torch.equal(ws[:16], before)
+    assert int(ws[:8].view(torch.int32)[0]) == 0 and int(ws[:8].view(torch.int32)[1]) == 0
+
+
+def test_unprepared_workspace_is_refused(cuda_device):
+    """A workspace that paged_attention_workspace_init never prepared:
+    PKV_EINVAL from pkv_check, no row written, and the next call works."""
+    c = PrefillCase(custom((300, 40), (300, 40), H=2, Hkv=2), cuda_device)
+    raw = torch.zeros(256, dtype=torch.uint8, device=cuda_device)
+    o = torch.full_like(c.q_dev, 7.0)
+    _prefill_abi(c, o, raw.data_ptr(), raw.numel())
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.check()
+    assert e.value.status == 1
+    assert (o == 7.0).all()
+    assert torch.equal(c.rerun(), c.out)
