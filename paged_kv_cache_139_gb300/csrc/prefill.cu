@@ -82,8 +82,9 @@ struct PfItem {
     int pad[5];
 };
 
-// Shared memory: the two query tiles, the K/V ring and two item slots.  P
-// stays in TMEM, over the tile's S columns.  The allocation keeps one CTA per
+// Shared memory: the two query tiles, the K/V ring, two item slots and a
+// 4 KB buffer per softmax warp through which its output rows go to global
+// memory as whole lines.  P stays in TMEM, over the tile's S columns.  The allocation keeps one CTA per
 // SM (each CTA takes all 512 TMEM columns).
 template <int D> struct PfLayout {
     static constexpr int NP = D / 64;                              // panels of d
@@ -92,7 +93,8 @@ template <int D> struct PfLayout {
     static constexpr uint32_t v = k + kStages * NP * kPanelBytes;
     static constexpr uint32_t bars = v + kStages * NP * kPanelBytes;
     static constexpr uint32_t items = bars + 256;
-    static constexpr uint32_t bytes = items + 2 * sizeof(PfItem);
+    static constexpr uint32_t stage = items + 2 * sizeof(PfItem);   // kTiles x kSoftmaxWarps x 4 KB
+    static constexpr uint32_t bytes = stage + kTiles * kSoftmaxWarps * 4096;
     static constexpr size_t alloc = (bytes + 1024 > 120u * 1024u) ? bytes + 1024 : 120u * 1024u;
 };
 
@@ -574,13 +576,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc::fence_after();
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-            T *orow = reinterpret_cast<T *>(a.out) + ((size_t)(it.q_begin + it.t0 + x * kRows + r) * a.num_heads + it.h) * D;
+            // Each 64-column panel of the warp's 32 rows goes through the warp's buffer: every
+            // thread writes its row (16-byte units swizzled by row, free of bank conflicts), then
+            // each store instruction writes 4 whole 128-byte row segments.
+            uint8_t *wb = sm + L::stage + (uint32_t)warp * 4096u;
+            const int wrow0 = 32 * (warp % 4);              // the warp's first tile row
+            T *obase = reinterpret_cast<T *>(a.out) + ((size_t)(it.q_begin + it.t0 + x * kRows) * a.num_heads + it.h) * D;
+            const size_t rstride = (size_t)a.num_heads * D;
 #pragma unroll
-            for (int c = 0; c < D / 32; c++) {
-                uint32_t o[32];
-                tc::tmem_ld32(tO + 32 * c, o);
-                tc::tmem_wait_ld(o);
-                if (r < rows_x) {
+            for (int p = 0; p < NP; p++) {
+#pragma unroll
+                for (int c = 0; c < 2; c++) {
+                    uint32_t o[32];
+                    tc::tmem_ld32(tO + 64 * p + 32 * c, o);
+                    tc::tmem_wait_ld(o);
 #pragma unroll
                     for (int v = 0; v < 4; v++) {
                         uint4 w;
@@ -588,9 +597,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         w.y = pack16<T>(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
                         w.z = pack16<T>(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
                         w.w = pack16<T>(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-                        *reinterpret_cast<uint4 *>(orow + 32 * c + 8 * v) = w;
+                        const int unit = 4 * c + v;
+                        *reinterpret_cast<uint4 *>(wb + lane * 128 + ((unit ^ (lane & 7)) << 4)) = w;
                     }
                 }
+                __syncwarp();
+#pragma unroll
+                for (int qq = 0; qq < 8; qq++) {
+                    const int lr = 4 * qq + (lane >> 3), unit = lane & 7;
+                    const uint4 w = *reinterpret_cast<const uint4 *>(wb + lr * 128 + ((unit ^ (lr & 7)) << 4));
+                    const int trow = wrow0 + lr;
+                    if (trow < rows_x) *reinterpret_cast<uint4 *>(obase + (size_t)trow * rstride + 64 * p + 8 * unit) = w;
+                }
+                __syncwarp();
             }
         }
         if (!ok && lane == 0) latch(st, kFlagTimeout, 2000000 + 1000 * k + j);
