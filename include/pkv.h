@@ -257,7 +257,10 @@ size_t paged_attention_workspace_size(int num_seqs, int num_heads, int num_kv_he
 pkv_status paged_attention_workspace_init(void *workspace_dev, size_t workspace_bytes,
                                           struct CUstream_st *stream);
 
-/* The partition size paged_attention_decode uses for these arguments. */
+/* The partition size paged_attention_decode uses for these arguments:
+ * partition_size when positive, else 512 tokens at head_dim 128 and 2048 at
+ * head_dim 64 (the same bytes per work item), halved down to 512 while
+ * num_seqs x num_kv_heads x ceil(max_context_len / P) stays below 2048. */
 int paged_attention_partition_size(int num_seqs, int num_heads, int num_kv_heads,
                                    int head_dim, int max_context_len, int partition_size);
 

@@ -144,3 +144,15 @@ def test_validate_copy_pairs(pairs, ok):
     else:
         with pytest.raises(pkv.PkvError):
             pkv.validate_copy_pairs(pairs, 8)
+
+
+def test_default_partition_size_follows_head_dim():
+    """512 tokens at head_dim 128; 2048 at head_dim 64 (the same bytes per
+    work item) unless that leaves fewer than 2048 items; an explicit size
+    always wins."""
+    f = _lib.load().paged_attention_partition_size
+    assert f(256, 32, 32, 128, 4096, 0) == 512
+    assert f(256, 32, 32, 64, 4096, 0) == 2048
+    assert f(16, 32, 32, 64, 4096, 0) == 1024      # 16 x 32 x 4 = 2048 items at 1024
+    assert f(1, 8, 8, 64, 32768, 0) == 512         # too few items at 1024 and 2048
+    assert f(256, 32, 32, 64, 4096, 256) == 256
