@@ -12,14 +12,18 @@
 // plain prompt; with fewer new tokens the first tokens are a cached prefix.
 //
 // How (sm_103a):
-//   * One CTA per (256 new tokens, query head, sequence): two query tiles of
-//     128 rows (M of both products) that take turns on the tensor core.  The
-//     grid walks a sequence's tiles from the last (the most keys) to the first.
-//   * A producer warp loads the query tiles (tiled TMA over the query tensor)
-//     and then, for each 128-key tile, the tile's K and V blocks (tiled TMA
-//     over the cache, one box of B tokens x 64 elements per block and
-//     64-element panel of d) into a two-stage ring.  Boxes land 128-byte
-//     swizzled, the layout the MMA descriptors describe.
+//   * Work items: (sequence, query head, 256 new tokens) = two query tiles of
+//     128 rows (M of both products) that take turns on the tensor core.  One
+//     persistent CTA per SM takes items from a ticket counter in the caller's
+//     workspace (without one, every gridDim-th ticket), the pairs of tiles
+//     with the most keys first.
+//   * A producer warp claims and looks up the next item while the current one
+//     streams and hands it to the other warps through a two-slot item ring; it
+//     loads each item's query tiles (tiled TMA over the query tensor) and then,
+//     for each 128-key tile, the tile's K and V blocks (tiled TMA over the
+//     cache, one box of B tokens x 64 elements per block and 64-element panel
+//     of d) into a two-stage ring that runs on across items.  Boxes land
+//     128-byte swizzled, the layout the MMA descriptors describe.
 //   * One thread of the MMA warp issues tcgen05.mma: S = Q K^T (M 128, N 128,
 //     fp32 in TMEM), then O += P V with P read from TMEM and V read MN-major
 //     straight from the cache layout (N = d: one product per 16 keys).  While one tile's
@@ -30,7 +34,8 @@
 //     probabilities stay below 2^8), write P as 16-bit over the scores in
 //     TMEM (for bf16 as a rounded part and its remainder) and rescale O in
 //     TMEM when a row's reference moved.  At the end they divide by the sum
-//     and store the rows.
+//     and write the rows through a per-warp shared-memory buffer, so that
+//     each store covers whole 128-byte row segments.
 //   * All waits are bounded; a wait that gives up latches a timeout, the CTA
 //     drains its copies and MMAs and frees its TMEM.
 #include <cfloat>
