@@ -225,8 +225,9 @@ def paged_attention_prefill(out: torch.Tensor, query: torch.Tensor, key_cache: t
     tokens of sequence s are the last n_s of its context_lens[s] and each
     attends every token up to its own position.  Their keys and values must
     already be in the cache.  workspace: a buffer from make_workspace (its
-    counter balances the work over the SMs); None takes the binding's own.
-    Returns out."""
+    counter balances the work over the SMs), serving one call at a time; None
+    takes the binding's own per-device buffer, which paged_attention_decode
+    calls share (calls through it must not overlap on the GPU).  Returns out."""
     T, H, d = query.shape
     NB, Hkv, B, d2 = key_cache.shape
     S = context_lens.shape[0]
