@@ -542,8 +542,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fence_proxy_async_smem();                // generic writes -> tensor-core reads
                 }
                 // pass 2, probabilities written over the scores
-                const float neg_m = -m_run;
-                float ls[4] = {0.f, 0.f, 0.f, 0.f};
+                // exponents and row sums two lanes at a time (packed fp32 pairs)
+                const unsigned long long c2x2 = pack2(c2, c2), negm2 = pack2(-m_run, -m_run);
+                unsigned long long ls2[2] = {0ull, 0ull};
 #pragma unroll
                 for (int c = 0; c < 4; c++) {
                     uint32_t (&sc)[32] = sb[c & 1];
@@ -553,13 +554,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t pk[kBf16 ? 32 : 16];
 #pragma unroll
                     for (int i = 0; i < 32; i += 2) {
-                        float p0 = fast_exp2(fmaf(__uint_as_float(sc[i]), c2, neg_m));
-                        float p1 = fast_exp2(fmaf(__uint_as_float(sc[i + 1]), c2, neg_m));
+                        const unsigned long long xx =
+                            fma2(pack2(__uint_as_float(sc[i]), __uint_as_float(sc[i + 1])), c2x2, negm2);
+                        float p0 = fast_exp2(lo2(xx));
+                        float p1 = fast_exp2(hi2(xx));
                         if (!full) {
                             p0 = kc + i <= lim ? p0 : 0.f;
                             p1 = kc + i + 1 <= lim ? p1 : 0.f;
                         }
-                        ls[(i >> 1) & 3] += p0 + p1;
+                        ls2[(i >> 1) & 1] = add2(ls2[(i >> 1) & 1], pack2(p0, p1));
                         const uint32_t hi = pack16<T>(p0, p1);
                         pk[i / 2] = hi;
                         // remainder after rounding (bf16 widens exactly by a shift)
@@ -570,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if constexpr (kBf16) tc::tmem_st32(tS + kc, pk);
                     else tc::tmem_st16(tS + kc, pk);
                 }
-                l_run = l_run * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+                l_run = l_run * alpha + ((lo2(ls2[0]) + hi2(ls2[0])) + (lo2(ls2[1]) + hi2(ls2[1])));
                 tc::tmem_wait_st();
                 tc::fence_before();
                 mbar_arrive(&bars[bPFull + x]);
