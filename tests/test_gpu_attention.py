@@ -57,6 +57,18 @@ def test_llama7b_small(cuda_device, B):
     _check(Case(workloads.llama7b(block_size=B, num_seqs=12, max_ctx=1500), cuda_device), what=f"llama7b B={B}")
 
 
+@pytest.mark.parametrize("S,P", [(16, 1024), (4, 512)])
+def test_default_partition_d64_halves(cuda_device, S, P):
+    """At head_dim 64 the default partition starts at 2048 and halves while
+    fewer than 2048 work items would remain: 16 sequences x 32 heads take
+    1024, 4 take 512; both match the oracle."""
+    w = workloads.llama7b(block_size=16, head_dim=64, num_seqs=S)
+    mcl = int(w.context_lens.max())
+    assert pkv.paged_attention_partition_size(S, 32, 32, 64, mcl, 0) == P
+    c = Case(w, cuda_device, gen_device="cuda", subset=list(range(min(S, 4))))
+    _check(c, what=f"llama7b d=64 S={S}")
+
+
 @pytest.mark.parametrize("B,d", [(8, 128), (16, 128), (32, 128),
                                  # the block-size study: small and large blocks, small heads
                                  (4, 128), (128, 128), (4, 64), (16, 64), (64, 64), (128, 64)])
