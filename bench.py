@@ -13,7 +13,8 @@ divided by the step time.
 
 --workload prefix times the prompt phase instead: after a shared cached
 prefix, the copy-on-write of its last block, the cache write of every
-request's own tokens and causal prompt-phase attention, in TFLOP/s.
+request's own tokens and causal prompt-phase attention, in TFLOP/s
+(--block-size, --head-dim, --kv-heads and --dtype vary its shape).
 
 Prints one JSON line (rank 0).  Under torchrun each rank runs an independent
 replica (a different seed) on its own GPU; the value is all ranks' bytes over
@@ -60,6 +61,8 @@ def parse():
     ap.add_argument("--block-size", type=int, default=16)
     ap.add_argument("--head-dim", type=int, default=128, choices=[64, 128])
     ap.add_argument("--partition-size", type=int, default=-1)
+    ap.add_argument("--kv-heads", type=int, default=0, help="prefix workload: kv heads (0: MHA)")
+    ap.add_argument("--dtype", default="", choices=["", "f16", "bf16"], help="prefix workload: cache dtype")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -72,6 +75,13 @@ def make_workload(args, rank: int) -> workloads.Workload:
         kw["head_dim"] = args.head_dim
     if args.workload == "swap":
         kw["block_size"] = args.block_size
+    if args.workload == "prefix":
+        kw["block_size"] = args.block_size
+        kw["head_dim"] = args.head_dim
+        if args.kv_heads:
+            kw["num_kv_heads"] = args.kv_heads
+        if args.dtype:
+            kw["dtype"] = args.dtype
     if args.workload == "beam":
         kw["width"] = args.beam_width
     w = workloads.by_name(args.workload, **kw)
