@@ -124,22 +124,29 @@ def paged_attention_partition_size(num_seqs: int, num_heads: int, num_kv_heads: 
 
 def make_workspace(device, nbytes: int, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
     """A device buffer of at least nbytes, prepared for paged_attention_decode
-    (paged_attention_workspace_init)."""
+    and paged_attention_prefill (paged_attention_workspace_init).  Returns
+    once the preparation has finished, so any stream may use the buffer."""
     dev = torch.device(device)
     buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
-    _ck(load().paged_attention_workspace_init(buf.data_ptr(), buf.numel(), _stream(stream, dev)),
-        "paged_attention_workspace_init")
+    st = _stream(stream, dev)
+    _ck(load().paged_attention_workspace_init(buf.data_ptr(), buf.numel(), st), "paged_attention_workspace_init")
+    (stream or torch.cuda.current_stream(dev)).synchronize()
     return buf
 
 
 _ws_cache: dict = {}
+_ws_retired: list = []
 
 
 def _workspace(device, nbytes: int) -> torch.Tensor:
-    """The binding's own workspace: at least nbytes, kept per device."""
+    """The binding's own workspace: at least nbytes, kept per device.  A
+    buffer replaced by a larger one is kept alive, since calls on other
+    streams may still be using it (the sizes only grow, so few are kept)."""
     key = torch.device(device)
     buf = _ws_cache.get(key)
     if buf is None or buf.numel() < nbytes:
+        if buf is not None:
+            _ws_retired.append(buf)
         buf = make_workspace(key, nbytes)
         _ws_cache[key] = buf
     return buf

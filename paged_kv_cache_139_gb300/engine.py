@@ -159,6 +159,7 @@ class PagedKVCache:
         self.num_blocks, self.num_kv_heads, self.head_dim, self.block_size = shape[0], shape[1], shape[3], shape[2]
         self.max_blocks_per_seq = max_blocks_per_seq
         self._ws: Optional[torch.Tensor] = None
+        self._ws_retired: list = []
 
     # -- host bookkeeping ------------------------------------------------------
     def new_sequence(self, length: int) -> int:
@@ -228,6 +229,8 @@ class PagedKVCache:
         need = paged_attention_workspace_size(num_seqs, num_heads, self.num_kv_heads, self.head_dim,
                                               max_context_len, partition_size)
         if self._ws is None or self._ws.numel() < need:
+            if self._ws is not None:
+                self._ws_retired.append(self._ws)   # calls in flight on other streams may hold it
             self._ws = make_workspace(self.device, need)
         return self._ws
 
