@@ -137,7 +137,9 @@ pkv_status paged_attention_decode(void *out_dev, const void *query_dev,
  * new token, slot_mapping_dev[num_seqs] (int64) its slot, which must be the
  * slot of position context_lens[s] - 1 of sequence s's table (as the
  * allocator returns it); a negative slot writes nothing; a slot beyond the
- * pool latches PKV_EINDEX.  The result is that of kv_reshape_and_cache on
+ * pool, or any other slot than that position's (a slot the launch's other
+ * work items may be reading), latches PKV_EINDEX and is not written.  The
+ * result is that of kv_reshape_and_cache on
  * the same arguments followed by paged_attention_decode: the caches hold the
  * new tokens bit for bit and out is the attention over contexts that include
  * them.  When the batch takes the grid kernel (more than 4096 sequences) the
@@ -173,12 +175,16 @@ pkv_status paged_attention_decode_write(void *out_dev, const void *query_dev, co
  *   - Sizes whose partials would exceed 16 MiB (see
  *     paged_attention_workspace_size) return PKV_EINVAL, launching nothing.
  *   - The first call on each device looks up the array's device address and
- *     prepares its counters (no allocation; one small kernel on `stream`);
- *     make that first call before any stream capture.
+ *     prepares its counters (no allocation; one small kernel on `stream`,
+ *     which the call waits for).  pkv_check reporting PKV_ETIMEOUT marks the
+ *     array for preparation again, done the same way by the next call.  A
+ *     call that has to prepare the array while `stream` is capturing a CUDA
+ *     graph returns PKV_EINVAL and launches nothing: make the first call on
+ *     a device, and the first after a reported timeout, outside capture.
  *   - All calls on a device share the one array: calls that may overlap on
  *     the GPU (other streams, other threads) race and give wrong results; one
  *     call at a time per device.  Each completed call leaves the array ready
- *     for the next; after PKV_ETIMEOUT the library cannot reuse it.
+ *     for the next.
  * ------------------------------------------------------------------------- */
 pkv_status paged_attention_decode_noalloc(void *out_dev, const void *query_dev,
                                           const void *key_cache_dev, const void *value_cache_dev,

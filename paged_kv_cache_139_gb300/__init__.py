@@ -161,7 +161,10 @@ def paged_attention_decode(out: torch.Tensor, query: torch.Tensor, key_cache: to
     """out/query [S][H][d]; caches [NB][Hkv][B][d]; block_tables int32 [S][MB];
     context_lens int32 [S].  scale defaults to 1/sqrt(d).  A workspace passed
     in must come from make_workspace (or paged_attention_workspace_init) and
-    serve one call at a time.  Returns out."""
+    serve one call at a time; None takes the binding's own per-device buffer,
+    which every decode and prefill call without a workspace shares, so calls
+    through it must not overlap on the GPU (give calls on concurrent streams
+    a workspace each).  Returns out."""
     S, H, d = query.shape
     NB, Hkv, B, d2 = key_cache.shape
     if d2 != d or out.shape != query.shape or value_cache.shape != key_cache.shape:
@@ -195,7 +198,9 @@ def paged_attention_decode_write(out: torch.Tensor, query: torch.Tensor, key: to
                                  stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
     """kv_reshape_and_cache of each sequence's new token (key/value [S][Hkv][d],
     slot_mapping int64 [S], the slot of position context_lens[s] - 1) and
-    paged_attention_decode in one launch.  Returns out."""
+    paged_attention_decode in one launch.  workspace as for
+    paged_attention_decode: None shares the binding's per-device buffer, so
+    calls through it must not overlap on the GPU.  Returns out."""
     S, H, d = query.shape
     NB, Hkv, B, d2 = key_cache.shape
     if d2 != d or out.shape != query.shape or value_cache.shape != key_cache.shape:
@@ -265,7 +270,10 @@ def paged_attention_decode_noalloc(out: torch.Tensor, query: torch.Tensor, key_c
     """paged_attention_decode without a workspace: for callers that may not
     allocate device memory when they run attention.  The partition partials
     use the library's built-in 16 MiB device array, shared by every call on a
-    device (one call at a time); larger sizes raise PkvError (PKV_EINVAL)."""
+    device (one call at a time); larger sizes raise PkvError (PKV_EINVAL).
+    The first call on a device, and the first after check() reported a
+    device-wait timeout, prepares the array and waits for it, so it must not
+    run during stream capture (PkvError, PKV_EINVAL)."""
     S, H, d = query.shape
     NB, Hkv, B, d2 = key_cache.shape
     if d2 != d or out.shape != query.shape or value_cache.shape != key_cache.shape:

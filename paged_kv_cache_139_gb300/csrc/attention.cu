@@ -878,13 +878,24 @@ __global__ void __launch_bounds__(PConf<D, G, MMA>::THREADS, PConf<D, G, MMA>::C
                 // The step's new token of sequence s (position ctx - 1, in this partition): the
                 // producer writes its key and value rows for kv head g into the cache, then makes
                 // the writes visible to the copies below (every item that reads the slot writes it
-                // first; items of other kv heads or partitions never read it).
+                // first; items of other kv heads or partitions never read it).  That holds only for
+                // the slot of position ctx - 1 in the sequence's own table, so any other slot is
+                // latched and not written (it could race the copies of another item).
                 constexpr int VEC = D * (int)sizeof(T) / 16;       // 16-byte vectors per row
                 const long long slot = a.slots[s];
-                if (slot >= 0) {
+                if (slot >= 0) {                                    // uniform over the warp
                     const long long blk = slot >> a.log2_block;
+                    const int pos = tok0 + ntok - 1;                // -1 for an empty context
+                    const int lbl = pos >> a.log2_block;
+                    int own = -1;                                   // the table's block of position pos
+                    if (pos >= 0) {
+                        const int ew = __shfl_sync(kFull, ent, (lbl - win) & 31);
+                        own = lbl - win < 32 ? ew : __ldg(trow + lbl);
+                    }
                     if (blk >= a.num_blocks) {
                         if (lane == 0) latch(a.st, kFlagBadSlot, slot);
+                    } else if (pos < 0 || blk != (long long)own || (int)(slot & (B - 1)) != (pos & (B - 1))) {
+                        if (lane == 0) latch(a.st, kFlagSlotNotLast, slot);
                     } else if (lane < 2 * VEC) {
                         const int off = (int)(slot & (B - 1));
                         const int v = lane % VEC;

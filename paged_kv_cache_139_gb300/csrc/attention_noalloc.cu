@@ -28,13 +28,21 @@ static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void *g_scratch_addr[kMaxDevices] = {};
+struct Prepared {
+    void *addr;            // device address of g_scratch (null until the first call)
+    unsigned int epoch;    // pkv::timeout_epoch() when the counters were last prepared
+};
+Prepared g_prepared[kMaxDevices] = {};
 
-// Device address of g_scratch on the current device.  In host code the name
-// g_scratch is only a host-side stand-in for the symbol, never a device
-// address, so the address is looked up once per device and cached; the same
-// set-up prepares the array's counters (a kernel on the caller's stream,
-// ordered before the first attention launch).
+// Device address of g_scratch on the current device, with its counters
+// ready.  In host code the name g_scratch is only a host-side stand-in for
+// the symbol, never a device address, so the address is looked up once per
+// device and cached.  The counters are prepared on the first call and again
+// after pkv_check has reported a device-wait timeout (a kernel that gave up
+// may have left them mid-count): one zeroing kernel on `stream`, waited for
+// before the address is handed out, so that a later call on any stream finds
+// the array ready.  That preparation cannot be recorded into a CUDA graph, so
+// it is refused while `stream` is capturing.
 void *scratch_address(cudaStream_t stream, pkv_status *st) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
@@ -44,22 +52,45 @@ void *scratch_address(cudaStream_t stream, pkv_status *st) {
         return nullptr;
     }
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
+    Prepared &pr = g_prepared[dev];
+    const unsigned int epoch = pkv::timeout_epoch();
+    if (pr.addr && pr.epoch == epoch) return pr.addr;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(stream, &cs);
+    if (e != cudaSuccess) {
+        *st = pkv::fail(PKV_ECUDA, "paged_attention_decode_noalloc: stream capture status: %s", cudaGetErrorString(e));
+        return nullptr;
+    }
+    if (cs != cudaStreamCaptureStatusNone) {
+        *st = pkv::fail(PKV_EINVAL,
+                        "paged_attention_decode_noalloc: the built-in scratch of device %d must be prepared outside "
+                        "stream capture (make the first call on a device, and the first after pkv_check reported "
+                        "PKV_ETIMEOUT, before capturing)",
+                        dev);
+        return nullptr;
+    }
+    void *p = pr.addr;
+    if (!p) {
         e = cudaGetSymbolAddress(&p, g_scratch);
         if (e != cudaSuccess || !p) {
             *st = pkv::fail(PKV_ECUDA, "paged_attention_decode_noalloc: scratch address on device %d: %s", dev,
                             cudaGetErrorString(e));
             return nullptr;
         }
-        const pkv_status ist = paged_attention_workspace_init(p, kScratchBytes, stream);
-        if (ist != PKV_OK) {
-            *st = ist;
-            return nullptr;
-        }
-        g_scratch_addr[dev] = p;
     }
-    return g_scratch_addr[dev];
+    const pkv_status ist = paged_attention_workspace_init(p, kScratchBytes, stream);
+    if (ist != PKV_OK) {
+        *st = ist;
+        return nullptr;
+    }
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) {
+        *st = pkv::fail(PKV_ECUDA, "paged_attention_decode_noalloc: preparing the scratch: %s", cudaGetErrorString(e));
+        return nullptr;
+    }
+    pr.addr = p;
+    pr.epoch = epoch;
+    return p;
 }
 
 }  // namespace

@@ -28,6 +28,7 @@ enum : unsigned int {
     kFlagTimeout = 8u,         // a bounded wait gave up
     kFlagBadContext = 16u,     // context length negative or beyond the table
     kFlagBadWorkspace = 32u,   // attention workspace not initialised
+    kFlagSlotNotLast = 64u,    // fused decode write: slot is not position context_len - 1 of its table
 };
 
 __device__ __forceinline__ void latch(DeviceStatus *st, unsigned int flag, long long value) {

@@ -17,4 +17,10 @@ pkv_status fail(pkv_status st, const char *fmt, ...)
 // Count `n` kernel launches made by the library.
 void count_launches(int n);
 
+// How many times pkv_check has reported (and cleared) a device-wait timeout
+// on the current device.  A kernel that gave up may leave the work-ticket
+// counters of its workspace mid-count, so scratch the library prepares itself
+// is prepared again whenever this number changes.
+unsigned int timeout_epoch();
+
 }  // namespace pkv

@@ -23,6 +23,8 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 DeviceStatus *g_status_addr[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
+// Device-wait timeouts pkv_check has reported and cleared, per device.
+std::atomic<unsigned int> g_timeout_epoch[kMaxDevices];
 
 int current_device() {
     int d = 0;
@@ -66,6 +68,12 @@ DeviceStatus *status_ptr() {
     return g_status_addr[d];
 }
 
+unsigned int timeout_epoch() {
+    int d = current_device();
+    if (d < 0 || d >= kMaxDevices) return 0;
+    return g_timeout_epoch[d].load(std::memory_order_acquire);
+}
+
 int sm_count() {
     int d = current_device();
     if (d < 0 || d >= kMaxDevices) return 0;
@@ -86,7 +94,7 @@ const char *pkv_last_error_string(void) { return pkv::t_msg; }
 
 uint64_t pkv_launch_count(void) { return pkv::g_launches.load(std::memory_order_relaxed); }
 
-int pkv_version(void) { return 106; }
+int pkv_version(void) { return 107; }
 
 pkv_status pkv_check(struct CUstream_st *stream) {
     cudaError_t e = cudaStreamSynchronize(stream);
@@ -95,6 +103,11 @@ pkv_status pkv_check(struct CUstream_st *stream) {
     e = cudaMemcpyFromSymbol(&h, pkv::g_status, sizeof h);
     if (e != cudaSuccess) return pkv::fail(PKV_ECUDA, "pkv_check: reading status: %s", cudaGetErrorString(e));
     if (h.flags == 0) return PKV_OK;
+    if (h.flags & pkv::kFlagTimeout) {
+        // a kernel that gave up may have left work-ticket counters mid-count
+        const int d = pkv::current_device();
+        if (d >= 0 && d < pkv::kMaxDevices) pkv::g_timeout_epoch[d].fetch_add(1u, std::memory_order_acq_rel);
+    }
     pkv::DeviceStatus zero;
     std::memset(&zero, 0, sizeof zero);
     e = cudaMemcpyToSymbol(pkv::g_status, &zero, sizeof zero);
@@ -106,6 +119,8 @@ pkv_status pkv_check(struct CUstream_st *stream) {
                        : (h.first_flag & pkv::kFlagBadBlock)   ? "block-table entry outside the pool"
                        : (h.first_flag & pkv::kFlagBadPair)    ? "copy pair outside the pool"
                        : (h.first_flag & pkv::kFlagBadContext) ? "context length outside the table"
+                       : (h.first_flag & pkv::kFlagSlotNotLast)
+                           ? "decode slot is not position context_len - 1 of its sequence's block table"
                        : (h.first_flag & pkv::kFlagTimeout)    ? "device wait timed out"
                                                                : "unknown";
     pkv_status st = (h.flags & ~pkv::kFlagTimeout) ? PKV_EINDEX : PKV_ETIMEOUT;

@@ -2,11 +2,14 @@
 library (native allocator + kernels, on the GPU) and once through the oracle
 (reference allocator, oracle cache write / copy / attention, on the CPU).
 
-For large workloads the oracle side works on a subset of the sequences: the
-physical blocks those sequences reference are gathered (from the pre-write
-input pool) into a compact pool with renumbered tables and slots.  A written
-block always belongs to its writer alone (copy-on-write), so the subset's
-blocks are not touched by the other sequences' writes.
+For large workloads the oracle side works on a subset of the sequences, of
+the kv heads, or both: the physical blocks those sequences reference are
+gathered (from the pre-write input pool) into a compact pool with renumbered
+tables and slots, keeping only the chosen kv heads (and the query heads that
+read them).  A written block always belongs to its writer alone
+(copy-on-write), so the subset's blocks are not touched by the other
+sequences' writes; heads never mix in attention, so a head subset computes
+exactly the rows it keeps.
 """
 from __future__ import annotations
 
@@ -61,9 +64,15 @@ class Case:
     oracle side on demand (oracle_out)."""
 
     def __init__(self, w: workloads.Workload, device="cuda", gen_device="cpu",
-                 subset: Optional[list] = None, partition_size: Optional[int] = None, fused: bool = False):
+                 subset: Optional[list] = None, partition_size: Optional[int] = None, fused: bool = False,
+                 kv_heads: Optional[list] = None):
         self.fused = fused
         self.w = w
+        G = w.num_heads // w.num_kv_heads
+        self.kv_heads = None if kv_heads is None else sorted(int(g) for g in kv_heads)
+        # query heads the oracle computes (those reading the kept kv heads)
+        self.q_heads = (np.arange(w.num_heads) if self.kv_heads is None else
+                        np.array([g * G + j for g in self.kv_heads for j in range(G)], np.int64))
         self.device = torch.device(device)
         self.partition_size = w.partition_size if partition_size is None else partition_size
         t = workloads.tensors(w, device=gen_device)
@@ -114,9 +123,17 @@ class Case:
                     need.add(int(src))
             self.blocks = np.array(sorted(need), dtype=np.int64)
         idx = torch.from_numpy(self.blocks).to(self._pool_k.device)
-        self.o_kc = oracle.bits16(self._pool_k.index_select(0, idx))
-        self.o_vc = oracle.bits16(self._pool_v.index_select(0, idx))
+        pk, pv = self._pool_k.index_select(0, idx), self._pool_v.index_select(0, idx)
+        if self.kv_heads is not None:
+            hidx = torch.tensor(self.kv_heads, device=pk.device)
+            pk, pv = pk.index_select(1, hidx), pv.index_select(1, hidx)
+        self.o_kc = oracle.bits16(pk)
+        self.o_vc = oracle.bits16(pv)
         self.remap = {int(b): i for i, b in enumerate(self.blocks)}
+
+    def _kv_rows(self, x):
+        """New-token keys or values [T][Hkv][d] restricted to the kept kv heads."""
+        return x if self.kv_heads is None else x[:, self.kv_heads]
 
     # -- library side -------------------------------------------------------------
     def run_gpu(self):
@@ -191,13 +208,14 @@ class Case:
             if pr:
                 oracle.copy_blocks(kc, pr)
                 oracle.copy_blocks(vc, pr)
-            oracle.cache_write(self.suffix["key"], self.suffix["value"], kc, vc,
+            oracle.cache_write(self._kv_rows(self.suffix["key"]), self._kv_rows(self.suffix["value"]), kc, vc,
                                self._remap_slots(self.ref_sfx_slots))
         pr = self._remap_pairs(self.ref_pairs)
         if pr:
             oracle.copy_blocks(kc, pr)
             oracle.copy_blocks(vc, pr)
-        oracle.cache_write(self.key, self.value, kc, vc, self._remap_slots(self.ref_slots))
+        oracle.cache_write(self._kv_rows(self.key), self._kv_rows(self.value), kc, vc,
+                           self._remap_slots(self.ref_slots))
         self._o_done = True
         return kc, vc
 
@@ -210,21 +228,29 @@ class Case:
         return t
 
     def oracle_out(self, heads=None):
-        """fp64 [len(sel)][H][d]; `heads`: optional list of (row in sel, head)."""
+        """fp64 [len(sel)][len(q_heads)][d]; `heads`: optional list of (row in
+        sel, index in q_heads)."""
         kc, vc = self.oracle_caches()
         q = self.query[torch.from_numpy(self.sel).to(self.query.device)]
+        q = q[:, torch.from_numpy(self.q_heads).to(q.device)]
         return oracle.paged_attention(q, kc, vc, self.oracle_tables(), self.ref_ctx[self.sel],
                                       self.w.dtype, which=heads)
 
     def gpu_out(self, out=None):
+        """The library's output [len(sel)][len(q_heads)][d] as fp64."""
         o = self.out if out is None else out
-        return o.index_select(0, torch.from_numpy(self.sel).to(o.device)).double().cpu().numpy()
+        o = o.index_select(0, torch.from_numpy(self.sel).to(o.device))
+        return o.index_select(1, torch.from_numpy(self.q_heads).to(o.device)).double().cpu().numpy()
 
     def gpu_cache_blocks(self):
-        """The library's K/V pools after the step, restricted to the oracle's blocks."""
+        """The library's K/V pools after the step, restricted to the oracle's
+        blocks (and kv heads)."""
         idx = torch.from_numpy(self.blocks).to(self.device)
-        return (oracle.bits16(self.eng.key_cache.index_select(0, idx)),
-                oracle.bits16(self.eng.value_cache.index_select(0, idx)))
+        k, v = self.eng.key_cache.index_select(0, idx), self.eng.value_cache.index_select(0, idx)
+        if self.kv_heads is not None:
+            hidx = torch.tensor(self.kv_heads, device=self.device)
+            k, v = k.index_select(1, hidx), v.index_select(1, hidx)
+        return oracle.bits16(k), oracle.bits16(v)
 
 
 def assert_close(got: np.ndarray, want: np.ndarray, what: str = ""):

@@ -35,6 +35,12 @@ def _custom(name="custom", S=3, H=4, Hkv=2, d=128, B=16, dtype="f16", ctx=(1, 40
     return workloads.Workload(name, S, H, Hkv, d, B, dtype, ctx, mb, nb, seed, partition)
 
 
+def _head_sample(w, k):
+    """A seeded choice of k kv heads of the workload (the parity sample of a
+    full-size batch)."""
+    return sorted(np.random.default_rng(w.seed).choice(w.num_kv_heads, k, replace=False).tolist())
+
+
 def test_tiny_workload(cuda_device):
     c = Case(workloads.tiny(), cuda_device)
     _check(c, what="tiny")
@@ -73,10 +79,10 @@ def test_default_partition_d64_halves(cuda_device, S, P):
                                  # the block-size study: small and large blocks, small heads
                                  (4, 128), (128, 128), (4, 64), (16, 64), (64, 64), (128, 64)])
 def test_llama7b_full_sampled(cuda_device, B, d):
-    """The full 256 x uniform[1,4096] batch: all heads of 6 sampled sequences."""
+    """The full 256 x uniform[1,4096] batch in the default launch: every
+    sequence, on a seeded sample of 4 of the 32 heads."""
     w = workloads.llama7b(block_size=B, head_dim=d)
-    sel = [0, 17, 99, 128, 201, 255]
-    c = Case(w, cuda_device, gen_device="cuda", subset=sel)
+    c = Case(w, cuda_device, gen_device="cuda", kv_heads=_head_sample(w, 4))
     _check(c, what=f"llama7b full B={B} d={d}")
 
 
@@ -85,7 +91,10 @@ def test_sampling_small(cuda_device):
 
 
 def test_sampling_full_sampled(cuda_device):
-    c = Case(workloads.sampling(), cuda_device, subset=[0, 1, 2, 3, 101, 202, 255])
+    """The full 64 prompts x 4 samples batch (copy-on-write of the shared last
+    blocks, suffixes, decode step): every sequence, 4 sampled heads."""
+    w = workloads.sampling()
+    c = Case(w, cuda_device, kv_heads=_head_sample(w, 4))
     _check(c, what="sampling full")
 
 
@@ -94,12 +103,11 @@ def test_longgqa_small(cuda_device):
 
 
 def test_longgqa_full_sampled(cuda_device):
-    """8 x 32768 tokens, bf16, GQA 32/8, partitions of 512: sampled heads of
-    two sequences (the oracle computes them one by one)."""
+    """8 x 32768 tokens, bf16, GQA 32/8, partitions of 512: every sequence, on
+    the 8 query heads of 2 sampled kv heads."""
     w = workloads.longgqa()
-    c = Case(w, cuda_device, gen_device="cuda", subset=[0, 7])
-    heads = [(0, 0), (0, 3), (0, 17), (1, 30), (1, 31), (1, 4)]
-    _check(c, heads=heads, what="longgqa full")
+    c = Case(w, cuda_device, gen_device="cuda", kv_heads=_head_sample(w, 2))
+    _check(c, what="longgqa full")
 
 
 @pytest.mark.parametrize("H,Hkv", [(4, 4), (4, 2), (8, 2), (12, 4), (16, 2), (10, 2), (6, 6), (7, 1)])
@@ -379,3 +387,36 @@ def test_fused_write_bad_slot_latches_eindex(cuda_device):
     with pytest.raises(pkv.PkvError) as e:
         pkv.check()
     assert e.value.status == 3
+
+
+@pytest.mark.parametrize("where", ["other_partition", "other_sequence", "wrong_offset"])
+def test_fused_write_slot_contract_latched(cuda_device, where):
+    """paged_attention_decode_write only writes a slot that is position
+    context_len - 1 of the sequence's own table (no other work item of the
+    launch reads it).  A slot elsewhere -- in an earlier partition, in another
+    sequence's block, or at another offset of the right block -- is latched as
+    PKV_EINDEX and not written."""
+    w = _custom(H=4, Hkv=2, ctx=(5, 40, 1300), S=3)
+    c = Case(w, cuda_device, partition_size=256)
+    B = w.block_size
+    tables, ctx = c.plan.tables, c.plan.context_lens
+    s = 2
+    if where == "other_partition":
+        bad = int(tables[s][0]) * B + 3                   # position 3: partition 0 of 6
+    elif where == "other_sequence":
+        bad = int(tables[1][1]) * B + 7                   # sequence 1's second block
+    else:
+        last = int(ctx[s]) - 1
+        bad = int(tables[s][last // B]) * B + (last + 1) % B
+    slots = c.dev.slots.clone()
+    slots[s] = bad
+    kc0, vc0 = c.eng.key_cache.clone(), c.eng.value_cache.clone()
+    out = torch.empty_like(c.q_dev)
+    pkv.paged_attention_decode_write(out, c.q_dev, c.k_dev, c.v_dev, c.eng.key_cache, c.eng.value_cache, slots,
+                                     c.dev.tables, c.dev.context_lens, partition_size=256)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.check()
+    assert e.value.status == 3
+    assert "context_len - 1" in pkv._lib.load().pkv_last_error_string().decode()
+    bb = bad // B
+    assert torch.equal(c.eng.key_cache[bb], kc0[bb]) and torch.equal(c.eng.value_cache[bb], vc0[bb])

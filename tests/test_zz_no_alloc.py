@@ -6,9 +6,13 @@ partition partials live in the library's built-in device array.
 
 Checked through the C ABI against paged_attention_decode with a caller
 workspace, on two calls in a row (the array keeps the previous call's
-contents), within the tolerance of the other attention tests.  This file is
-collected last so that a run stopping at the first failure has already run
-every other test; it also passes on its own in a fresh process.
+contents).  Both entry points run the same kernels, whose results do not
+depend on which CTA takes which work item, so the outputs must be equal bit
+for bit -- a stale counter or a scratch overlap would show up here.  The
+array is prepared again after check() reported a device-wait timeout, and
+that preparation is refused during stream capture.  This file is collected
+last so that a run stopping at the first failure has already run every other
+test; it also passes on its own in a fresh process.
 """
 import ctypes
 
@@ -18,7 +22,6 @@ import torch
 
 import paged_kv_cache_139_gb300 as pkv
 import workloads
-from cases import assert_close
 from paged_kv_cache_139_gb300 import _lib
 
 pytestmark = pytest.mark.gpu
@@ -59,13 +62,68 @@ def test_noalloc_matches_workspace_entry(cuda_device, S, H, Hkv, d, B, ctx, dtyp
     ws = pkv.make_workspace(cuda_device, pkv.paged_attention_workspace_size(S, H, Hkv, d, bt.shape[1] * B, P))
     pkv.paged_attention_decode(ref, q, kc, vc, bt, cl, partition_size=P, workspace=ws)
     pkv.check()
-    want = ref.double().cpu().numpy()
     for call in range(2):
         out = torch.full_like(q, float("nan"))
         rc = _noalloc_raw(out, q, kc, vc, bt, cl, P)
         assert rc == 0, _lib.load().pkv_last_error_string()
         pkv.check()
-        assert_close(out.double().cpu().numpy(), want, f"noalloc call {call}")
+        assert torch.equal(out, ref), f"noalloc call {call} differs from the workspace entry point"
+
+
+def _latch_and_report_timeout():
+    s = torch.cuda.current_stream()
+    assert _lib.load().pkv_selftest_wait_timeout(1 << 20, ctypes.c_void_p(s.cuda_stream)) == 0
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.check()
+    assert e.value.status_name == "PKV_ETIMEOUT"
+
+
+def test_noalloc_prepared_again_after_a_reported_timeout(cuda_device):
+    """After check() has reported a device-wait timeout the next call prepares
+    the array again (a kernel that gave up may have left its counters
+    mid-count) and still matches the workspace entry point bit for bit."""
+    S, H, Hkv, d, B, ctx, P = 2, 32, 8, 128, 16, [4096, 3001], 512
+    q, kc, vc, bt, cl = _inputs(cuda_device, S, H, Hkv, d, B, ctx, "bf16", 29)
+    ref = torch.empty_like(q)
+    ws = pkv.make_workspace(cuda_device, pkv.paged_attention_workspace_size(S, H, Hkv, d, bt.shape[1] * B, P))
+    pkv.paged_attention_decode(ref, q, kc, vc, bt, cl, partition_size=P, workspace=ws)
+    pkv.check()
+    _latch_and_report_timeout()
+    for call in range(2):
+        out = torch.full_like(q, float("nan"))
+        assert _noalloc_raw(out, q, kc, vc, bt, cl, P) == 0, _lib.load().pkv_last_error_string()
+        pkv.check()
+        assert torch.equal(out, ref), f"call {call} after the timeout"
+
+
+def test_noalloc_preparation_refused_during_capture(cuda_device):
+    """A call that must prepare the array (here: the first after a reported
+    timeout) inside a CUDA-graph capture returns PKV_EINVAL and records
+    nothing; the next call outside capture prepares it and is correct."""
+    S, H, Hkv, d, B, ctx, P = 3, 8, 8, 64, 32, [700, 64, 2500], 128
+    q, kc, vc, bt, cl = _inputs(cuda_device, S, H, Hkv, d, B, ctx, "f16", 31)
+    ref = torch.empty_like(q)
+    ws = pkv.make_workspace(cuda_device, pkv.paged_attention_workspace_size(S, H, Hkv, d, bt.shape[1] * B, P))
+    pkv.paged_attention_decode(ref, q, kc, vc, bt, cl, partition_size=P, workspace=ws)
+    pkv.check()
+    # a first call prepares the array, then a reported timeout marks it for preparation again
+    out = torch.empty_like(q)
+    assert _noalloc_raw(out, q, kc, vc, bt, cl, P) == 0
+    pkv.check()
+    _latch_and_report_timeout()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    before = pkv.launch_count()
+    with torch.cuda.graph(g, stream=side):
+        out.zero_()
+        rc = _noalloc_raw(out, q, kc, vc, bt, cl, P)
+    assert rc == 1                                                # PKV_EINVAL
+    assert "capture" in _lib.load().pkv_last_error_string().decode()
+    assert pkv.launch_count() == before
+    out = torch.full_like(q, float("nan"))
+    assert _noalloc_raw(out, q, kc, vc, bt, cl, P) == 0, _lib.load().pkv_last_error_string()
+    pkv.check()
+    assert torch.equal(out, ref)
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(cuda_device):
