@@ -93,8 +93,10 @@ pkv_status kv_reshape_and_cache(const void *key_dev, const void *value_dev,
  * rounded to `dtype`.  n = 0 gives zeros.  scale is usually 1/sqrt(head_dim).
  *
  * Long contexts are split into partitions of partition_size tokens; each is
- * reduced to (max, sum of exponentials, un-normalised value sum) and a second
- * kernel merges them by log-sum-exp.  partition_size = 0 lets the library
+ * reduced to (max, sum of exponentials, un-normalised value sum) and the
+ * partitions are merged by log-sum-exp: inside the attention kernel for
+ * splits of up to 16 partitions, by a second kernel for longer ones.
+ * partition_size = 0 lets the library
  * choose; otherwise it must be a positive multiple of 32.
  *   max_context_len   host-side upper bound on every context_lens[s]
  *                     (0 = max_blocks_per_seq * block_size); a larger
@@ -105,9 +107,13 @@ pkv_status kv_reshape_and_cache(const void *key_dev, const void *value_dev,
  *   workspace_dev     at least paged_attention_workspace_size(...) bytes of
  *                     device scratch owned by the caller, initialised once
  *                     with paged_attention_workspace_init before its first
- *                     use.  Its head holds the work-ticket counters, which
- *                     every completed call leaves ready for the next; the
- *                     rest is clobbered.  Calls that may overlap on the GPU
+ *                     use.  It holds the work-ticket and merge counters,
+ *                     which every completed call leaves ready for the next,
+ *                     and the partition partials, which are clobbered.  The
+ *                     merge counters move with the call's sizes: a call whose
+ *                     sizes differ from the previous call's on the same
+ *                     workspace first zeroes them (one more small launch).
+ *                     Calls that may overlap on the GPU
  *                     need separate workspaces.  After a call that reported
  *                     PKV_ETIMEOUT, initialise it again.  An uninitialised
  *                     workspace makes the call do nothing and pkv_check

@@ -31,7 +31,9 @@
 #include <cudaTypedefs.h>
 
 #include <cfloat>
+#include <array>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <type_traits>
 
@@ -407,19 +409,22 @@ struct AttnArgs {
     const int64_t *slots;        // [S]
 };
 
-// splits of up to this many partitions merge inside the attention kernel;
-// longer ones go to partition_reduce_kernel (at most 32)
+// Splits of up to this many partitions merge inside the attention kernel:
+// the CTA that completes the last partition of a (sequence, query-head tile)
+// -- found by an atomic counter -- merges them.  Longer splits go to
+// partition_reduce_kernel.
 #ifndef PKV_FUSED_MAX_PARTS
 #define PKV_FUSED_MAX_PARTS 16
 #endif
 constexpr int kFusedMaxParts = PKV_FUSED_MAX_PARTS;
 static_assert(kFusedMaxParts <= 32, "the in-kernel merge keeps one partition per lane");
 
-// The partitions of query heads h0 .. h0 + G - 1 of sequence s, merged by one
-// warp (log-sum-exp, as partition_reduce_kernel) straight from the workspace.
-// Lane L owns D/32 consecutive elements; partial rows are read as vectors, 8
-// partitions at a time in flight.  The partials were written by other CTAs:
-// read them past L1.
+// Log-sum-exp merge, by one warp, of the np partitions of query heads
+// h0 .. h0 + G - 1 of sequence s (np <= 32, one per lane):
+// M = max m_p, L = sum l_p 2^(m_p - M), out = sum o_p 2^(m_p - M) / L.
+// Lane L owns D/32 consecutive elements of a row.  The partials were written
+// by other CTAs: they are read past L1.  A head's m, l and first 8 rows are
+// loaded together, so a head costs one round trip per 8 partitions.
 template <int D, int G, typename T>
 __device__ __forceinline__ void merge_partitions_warp(const AttnArgs &a, int s, int h0, int np, int lane) {
     constexpr int EPL = D / 32;
@@ -427,12 +432,11 @@ __device__ __forceinline__ void merge_partitions_warp(const AttnArgs &a, int s, 
     for (int h = 0; h < G; h++) {
         const size_t base = ((size_t)s * a.num_heads + h0 + h) * a.max_parts;
         const float mp = lane < np ? __ldcg(a.ws_m + base + lane) : -INFINITY;
-        const float M = warp_max(mp);
-        const float wp = lane < np ? exp2f(mp - M) : 0.f;
-        const float L = warp_sum(lane < np ? __ldcg(a.ws_l + base + lane) * wp : 0.f);
+        const float lp = lane < np ? __ldcg(a.ws_l + base + lane) : 0.f;
         float acc[EPL];
 #pragma unroll
         for (int k = 0; k < EPL; k++) acc[k] = 0.f;
+        float wp = 0.f;
 #pragma unroll 1
         for (int p0 = 0; p0 < np; p0 += 8) {
             float ov[8][EPL];
@@ -452,6 +456,10 @@ __device__ __forceinline__ void merge_partitions_warp(const AttnArgs &a, int s, 
                     for (int k = 0; k < EPL; k++) ov[j][k] = 0.f;
                 }
             }
+            if (p0 == 0) {                       // uniform: the weights, while the first rows load
+                const float M = warp_max(mp);
+                wp = lane < np ? exp2f(mp - M) : 0.f;
+            }
 #pragma unroll
             for (int j = 0; j < 8; j++) {
                 const float w = __shfl_sync(kFull, wp, (p0 + j) & 31);
@@ -459,6 +467,7 @@ __device__ __forceinline__ void merge_partitions_warp(const AttnArgs &a, int s, 
                 for (int k = 0; k < EPL; k++) acc[k] = fmaf(w, ov[j][k], acc[k]);
             }
         }
+        const float L = warp_sum(lp * wp);
         T *dst = static_cast<T *>(a.out) + ((size_t)s * a.num_heads + h0 + h) * D + lane * EPL;
 #pragma unroll
         for (int k = 0; k < EPL; k++) dst[k] = F16Traits<T>::from_f32(L > 0.f ? acc[k] / L : 0.f);
@@ -1192,21 +1201,26 @@ __global__ void __launch_bounds__(PConf<D, G, MMA>::THREADS, PConf<D, G, MMA>::C
 
 // Merge the partitions of each (sequence, head) with more than one:
 // M = max_p m_p, L = sum_p l_p 2^(m_p - M), out = sum_p o_p 2^(m_p - M) / L.
-// One CTA per (head, sequence); kReduceThreads / D groups of D threads split
-// the partitions between them (thread e of a group owns output element e),
-// so that many partial rows are in flight at once.
+// One CTA per (head, sequence).  Thread t owns the 16-byte column t % CPR of
+// the partial rows t / CPR, t / CPR + RG, ... of a chunk of RG * kReduceRows
+// partitions: a chunk's rows are all requested at once, before the weights
+// they need are known, so a split of up to one chunk (64 partitions at
+// head_dim 128) costs about two round trips to L2.
 constexpr int kReduceThreads = 256;
-constexpr int kReduceChunk = 1024;                  // partition weights staged per pass
+constexpr int kReduceRows = 8;                      // partial rows per thread per chunk
 
 template <int D, typename T>
 __global__ void __launch_bounds__(kReduceThreads) partition_reduce_kernel(const AttnArgs a) {
-    constexpr int NG = kReduceThreads / D;
-    __shared__ float wsh[kReduceChunk];
-    __shared__ float red[kReduceThreads / 32];
-    __shared__ float opart[NG][D];
+    constexpr int CPR = D / 4;                      // float4 columns per row
+    constexpr int RG = kReduceThreads / CPR;        // row groups
+    constexpr int CH = RG * kReduceRows;            // partitions per chunk
+    static_assert(CH <= kReduceThreads, "one weight per thread and chunk");
+    __shared__ float wsh[CH];
+    __shared__ float red[2][kReduceThreads / 32];
+    __shared__ float4 opart[RG][CPR];
     pdl_trigger();
     pdl_wait();
-    const int h = blockIdx.x, s = blockIdx.y, tid = threadIdx.x;
+    const int h = blockIdx.x, s = blockIdx.y, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     int ctx = a.ctx_lens[s];
     ctx = ctx < 0 ? 0 : (ctx > a.max_ctx ? a.max_ctx : ctx);
     const int np = (ctx + a.partition - 1) / a.partition;
@@ -1214,42 +1228,65 @@ __global__ void __launch_bounds__(kReduceThreads) partition_reduce_kernel(const 
     const size_t base = ((size_t)s * a.num_heads + h) * a.max_parts;
     const float *m = a.ws_m + base;
     const float *l = a.ws_l + base;
-    const float *o = a.ws_o + base * D;
-    // M
-    float mx = -INFINITY;
-    for (int p = tid; p < np; p += kReduceThreads) mx = fmaxf(mx, m[p]);
-    mx = warp_max(mx);
-    if ((tid & 31) == 0) red[tid >> 5] = mx;
-    __syncthreads();
-    float M = red[0];
+    const float4 *o = reinterpret_cast<const float4 *>(a.ws_o + base * D);
+    const int c = tid % CPR, rg = tid / CPR;
+    float4 ov[kReduceRows];
+    auto load_chunk = [&](int p0) {
 #pragma unroll
-    for (int w = 1; w < kReduceThreads / 32; w++) M = fmaxf(M, red[w]);
+        for (int k = 0; k < kReduceRows; k++) {
+            const int p = p0 + rg + RG * k;
+            ov[k] = p < np ? __ldcg(o + (size_t)p * CPR + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    };
+    // the first chunk's rows and the first kReduceThreads (m, l) are requested together
+    load_chunk(0);
+    const float m0 = tid < np ? __ldcg(m + tid) : -INFINITY;
+    const float l0 = tid < np ? __ldcg(l + tid) : 0.f;
+    float mx = m0;
+    for (int p = tid + kReduceThreads; p < np; p += kReduceThreads) mx = fmaxf(mx, __ldcg(m + p));
+    mx = warp_max(mx);
+    if (lane == 0) red[0][wid] = mx;
     __syncthreads();
-    const int grp = tid / D, e = tid % D;
-    float Lp = 0.f, O = 0.f;
-    for (int p0 = 0; p0 < np; p0 += kReduceChunk) {
-        const int n = np - p0 < kReduceChunk ? np - p0 : kReduceChunk;
-        for (int p = tid; p < n; p += kReduceThreads) {
-            const float wt = exp2f(m[p0 + p] - M);
-            wsh[p] = wt;
-            Lp = fmaf(l[p0 + p], wt, Lp);
+    float M = red[0][0];
+#pragma unroll
+    for (int w = 1; w < kReduceThreads / 32; w++) M = fmaxf(M, red[0][w]);
+    const float w0 = tid < np ? exp2f(m0 - M) : 0.f;
+    float lp = l0 * w0;
+    for (int p = tid + kReduceThreads; p < np; p += kReduceThreads)
+        lp = fmaf(__ldcg(l + p), exp2f(__ldcg(m + p) - M), lp);
+    lp = warp_sum(lp);
+    if (lane == 0) red[1][wid] = lp;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int p0 = 0; p0 < np; p0 += CH) {
+        if (p0 > 0) load_chunk(p0);
+        if (tid < CH) wsh[tid] = p0 == 0 ? w0 : (p0 + tid < np ? exp2f(__ldcg(m + p0 + tid) - M) : 0.f);
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < kReduceRows; k++) {
+            const float w = wsh[rg + RG * k];
+            acc.x = fmaf(w, ov[k].x, acc.x);
+            acc.y = fmaf(w, ov[k].y, acc.y);
+            acc.z = fmaf(w, ov[k].z, acc.z);
+            acc.w = fmaf(w, ov[k].w, acc.w);
         }
         __syncthreads();
-#pragma unroll 8
-        for (int p = grp; p < n; p += NG) O = fmaf(wsh[p], o[(size_t)(p0 + p) * D + e], O);
-        __syncthreads();
     }
-    Lp = warp_sum(Lp);
-    if ((tid & 31) == 0) red[tid >> 5] = Lp;
-    opart[grp][e] = O;
+    opart[rg][c] = acc;
     __syncthreads();
-    if (grp == 0) {
+    if (rg == 0) {
         float L = 0.f;
 #pragma unroll
-        for (int w = 0; w < kReduceThreads / 32; w++) L += red[w];
+        for (int w = 0; w < kReduceThreads / 32; w++) L += red[1][w];
 #pragma unroll
-        for (int g = 1; g < NG; g++) O += opart[g][e];
-        static_cast<T *>(a.out)[((size_t)s * a.num_heads + h) * D + e] = F16Traits<T>::from_f32(L > 0.f ? O / L : 0.f);
+        for (int g = 1; g < RG; g++) {
+            const float4 x = opart[g][c];
+            acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+        }
+        T *dst = static_cast<T *>(a.out) + ((size_t)s * a.num_heads + h) * D + c * 4;
+        dst[0] = F16Traits<T>::from_f32(L > 0.f ? acc.x / L : 0.f);
+        dst[1] = F16Traits<T>::from_f32(L > 0.f ? acc.y / L : 0.f);
+        dst[2] = F16Traits<T>::from_f32(L > 0.f ? acc.z / L : 0.f);
+        dst[3] = F16Traits<T>::from_f32(L > 0.f ? acc.w / L : 0.f);
     }
 }
 
@@ -1276,7 +1313,8 @@ struct WsLayout {
 };
 
 // Workspace: the ticket header, then (when contexts may span partitions)
-// m, l [S][H][MP] and o [S][H][MP][D], each 256-byte aligned.
+// m, l [S][H][MP], o [S][H][MP][D] and the merge counters [S][H], each
+// region 256-byte aligned.
 WsLayout ws_layout(int S, int H, int D, int MP) {
     WsLayout w{};
     w.bytes = kWsHeaderBytes;
@@ -1296,6 +1334,34 @@ __global__ void workspace_init_kernel(uint4 *ws, size_t n16) {
     pdl_wait();
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x)
         ws[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+// The merge counters of a call sit after its partials, at offsets that
+// depend on the call's sizes, so a region that one call used for partials may
+// be another call's counters.  Every completed call leaves its own counters at
+// zero; the library remembers, per workspace, the layout of the last call
+// (a freshly initialised workspace is all zero) and zeroes the counter
+// regions before a call whose layout differs.
+using WsSig = std::array<int, 6>;                 // S, H, Hkv, D, MP, fused merge
+const WsSig kWsClean = {0, 0, 0, 0, 0, 0};
+std::mutex g_ws_mu;
+std::map<std::pair<int, uintptr_t>, WsSig> g_ws_last;
+
+int current_dev() {
+    int d = -1;
+    return cudaGetDevice(&d) == cudaSuccess ? d : -1;
+}
+
+void ws_remember(const void *ws, const WsSig &sig) {
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    g_ws_last[{current_dev(), reinterpret_cast<uintptr_t>(ws)}] = sig;
+}
+
+// True unless the workspace is known to hold zero counters for this layout.
+bool ws_counters_stale(const void *ws, const WsSig &sig) {
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    auto it = g_ws_last.find({current_dev(), reinterpret_cast<uintptr_t>(ws)});
+    return it == g_ws_last.end() || (it->second != sig && it->second != kWsClean);
 }
 
 __global__ void workspace_magic_kernel(WsHeader *h) {
@@ -1427,6 +1493,7 @@ pkv_status paged_attention_workspace_init(void *workspace, size_t workspace_byte
     if (e == cudaSuccess)
         e = launch(workspace_magic_kernel, dim3(1), dim3(1), 0, stream, static_cast<WsHeader *>(workspace));
     if (e != cudaSuccess) return fail(PKV_ECUDA, "paged_attention_workspace_init: launch: %s", cudaGetErrorString(e));
+    ws_remember(workspace, kWsClean);
     return PKV_OK;
 }
 
@@ -1529,9 +1596,21 @@ pkv_status decode_impl(void *out, const void *query, const void *key_cache, cons
     a.fused_merge = persistent && MP > 1 && MP <= kFusedMaxParts;
 
     const dim3 grid((unsigned)(num_kv_heads * a.head_tiles), (unsigned)num_seqs, (unsigned)MP);
-    cudaError_t e = dtype == PKV_F16 ? dispatch_d<__half>(head_dim, G, a, grid, stream)
-                                     : dispatch_d<__nv_bfloat16>(head_dim, G, a, grid, stream);
+    const WsSig sig = {num_seqs, num_heads, num_kv_heads, head_dim, MP, a.fused_merge};
+    cudaError_t e = cudaSuccess;
+    if (a.fused_merge && ws_counters_stale(workspace, sig)) {
+        // the counter regions (16-byte multiples: every region is 256-byte aligned)
+        const size_t n16 = (wl.bytes - wl.cnt_off) / 16;
+        long long blocks = (long long)((n16 + 255) / 256);
+        if (blocks > sm_count()) blocks = sm_count() > 0 ? sm_count() : 1;
+        e = launch(workspace_init_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
+                   reinterpret_cast<uint4 *>(ws + wl.cnt_off), n16);
+        if (e != cudaSuccess) return fail(PKV_ECUDA, "paged_attention_decode: counter reset: %s", cudaGetErrorString(e));
+    }
+    e = dtype == PKV_F16 ? dispatch_d<__half>(head_dim, G, a, grid, stream)
+                         : dispatch_d<__nv_bfloat16>(head_dim, G, a, grid, stream);
     if (e != cudaSuccess) return fail(PKV_ECUDA, "paged_attention_decode: launch: %s", cudaGetErrorString(e));
+    ws_remember(workspace, sig);
     if (MP > 1 && !a.fused_merge) {
         const dim3 rgrid((unsigned)num_heads, (unsigned)num_seqs);
         e = dtype == PKV_F16 ? launch_reduce<__half>(head_dim, a, rgrid, stream)

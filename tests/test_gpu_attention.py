@@ -134,6 +134,22 @@ def test_partition_sizes_agree(cuda_device, P):
     _check(c, what=f"P={P}")
 
 
+@pytest.mark.parametrize("H,Hkv,d,dtype", [(8, 2, 128, "f16"), (32, 8, 128, "bf16"), (4, 4, 64, "f16"),
+                                         (16, 2, 64, "bf16")])
+def test_merge_kernel_chunks(cuda_device, H, Hkv, d, dtype):
+    """Splits into 1, 16, 17, 24, 25, 64, 65, 255 and 256 partitions of 32
+    tokens, merged by partition_reduce_kernel in chunks of 64 (head_dim 128)
+    or 128 (head_dim 64) partitions, against the oracle; a second call is
+    bit-identical."""
+    w = _custom(H=H, Hkv=Hkv, d=d, dtype=dtype, ctx=(1, 512, 520, 768, 790, 2048, 2050, 8150, 8192), S=9)
+    c = Case(w, cuda_device, partition_size=32)
+    before = pkv.launch_count()
+    again = c.rerun_attention().clone()
+    assert pkv.launch_count() - before == 2
+    assert torch.equal(again, c.out)
+    _check(c, what=f"merge kernel H={H} Hkv={Hkv} d={d}")
+
+
 def test_context_zero_and_one(cuda_device):
     w = _custom(ctx=(1, 2, 1, 40), S=4)
     c = Case(w, cuda_device)
@@ -420,3 +436,41 @@ def test_fused_write_slot_contract_latched(cuda_device, where):
     assert "context_len - 1" in pkv._lib.load().pkv_last_error_string().decode()
     bb = bad // B
     assert torch.equal(c.eng.key_cache[bb], kc0[bb]) and torch.equal(c.eng.value_cache[bb], vc0[bb])
+
+
+def _rand_batch(dev, S, H, Hkv, d, B, ctx, dtype, seed):
+    ctx = np.asarray(ctx, np.int32)
+    mb = int(-(-int(ctx.max()) // B))
+    nb = S * mb
+    q = workloads.normal((S, H, d), dtype, seed).to(dev)
+    kc = workloads.normal((nb, Hkv, B, d), dtype, seed + 1).to(dev)
+    vc = workloads.normal((nb, Hkv, B, d), dtype, seed + 2).to(dev)
+    perm = np.random.default_rng(seed).permutation(nb).astype(np.int32).reshape(S, mb)
+    return q, kc, vc, torch.from_numpy(perm).to(dev), torch.from_numpy(ctx).to(dev)
+
+
+def test_workspace_shared_by_calls_of_different_sizes(cuda_device):
+    """One workspace serving calls of different sizes: the second call's merge
+    counters sit where the first call left partials, so the library zeroes
+    them when the sizes change.  Every call matches the same call on a fresh
+    workspace bit for bit, in both orders and again."""
+    a = _rand_batch(cuda_device, 4, 8, 8, 128, 16, [4000, 4096, 3900, 4050], "f16", 41)    # 16 partitions of 256
+    b = _rand_batch(cuda_device, 2, 8, 8, 128, 16, [1000, 900], "f16", 43)                 # 4 partitions of 256
+
+    def need(x):
+        q, kc, vc, bt, cl = x
+        return pkv.paged_attention_workspace_size(q.shape[0], q.shape[1], kc.shape[1], q.shape[2],
+                                                  bt.shape[1] * kc.shape[2], 256)
+
+    def run(x, ws):
+        q, kc, vc, bt, cl = x
+        out = torch.full_like(q, float("nan"))
+        pkv.paged_attention_decode(out, q, kc, vc, bt, cl, partition_size=256, workspace=ws)
+        pkv.check()
+        return out
+
+    want_a = run(a, pkv.make_workspace(cuda_device, need(a)))
+    want_b = run(b, pkv.make_workspace(cuda_device, need(b)))
+    ws = pkv.make_workspace(cuda_device, max(need(a), need(b)))
+    for x, want in [(a, want_a), (b, want_b), (a, want_a), (a, want_a), (b, want_b)]:
+        assert torch.equal(run(x, ws), want)
