@@ -48,6 +48,7 @@ SWAP_METRIC = "swap GB/s (KV blocks GPU -> pinned host -> GPU, both directions)"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 512 << 20
+L2_BYTES = 129e6                 # GB300 L2 (nominal)
 
 
 def parse():
@@ -62,6 +63,7 @@ def parse():
     ap.add_argument("--block-size", type=int, default=16)
     ap.add_argument("--head-dim", type=int, default=128, choices=[64, 128])
     ap.add_argument("--partition-size", type=int, default=-1)
+    ap.add_argument("--num-seqs", type=int, default=0, help="opt13b / llama7b: batch size (0: the workload's)")
     ap.add_argument("--kv-heads", type=int, default=0, help="prefix workload: kv heads (0: MHA)")
     ap.add_argument("--dtype", default="", choices=["", "f16", "bf16"], help="prefix workload: cache dtype")
     ap.add_argument("--no-e2e", action="store_true")
@@ -74,6 +76,8 @@ def make_workload(args, rank: int) -> workloads.Workload:
     if args.workload == "llama7b":
         kw["block_size"] = args.block_size
         kw["head_dim"] = args.head_dim
+    if args.workload in ("llama7b", "opt13b") and args.num_seqs > 0:
+        kw["num_seqs"] = args.num_seqs
     if args.workload == "swap":
         kw["block_size"] = args.block_size
     if args.workload == "prefix":
@@ -195,10 +199,13 @@ SAMPLE_KV_BYTES = 1 << 30        # KV held by the CPU baseline's sample of seque
 
 def decode_config(w: workloads.Workload, kv_bytes: int, world: int) -> dict:
     """The workload as both arms print it (identical keys and values)."""
-    return {**w.describe(),
-            "l2": f"KV per step {kv_bytes / 1e9:.2f} GB against a 129 MB L2; the GPU arm also flushes it before "
-                  f"every step ({L2_FLUSH_BYTES >> 20} MiB memset, outside the timed events)",
-            "kv_bytes_per_step": kv_bytes, "parallelism": f"replicas x{world}"}
+    if kv_bytes >= 4 * L2_BYTES:
+        l2 = (f"inputs larger than L2: {kv_bytes / 1e9:.2f} GB of KV per step against a 129 MB L2, steps back to "
+              f"back (the GPU arm's l2_flushed_each_step repeats them with a {L2_FLUSH_BYTES >> 20} MiB memset "
+              f"before each)")
+    else:
+        l2 = f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB memset, outside the timed events)"
+    return {**w.describe(), "l2": l2, "kv_bytes_per_step": kv_bytes, "parallelism": f"replicas x{world}"}
 
 
 def sample_sequences(w: workloads.Workload, ctx: np.ndarray, max_bytes: int = SAMPLE_KV_BYTES) -> list:
@@ -407,6 +414,31 @@ def sampling_setup(eng, w: workloads.Workload, dev):
                  "note": "both copy_blocks launches (K and V) of the suffix step, L2 flushed before"}
 
 
+def time_loop(stream, fn, n: int, flush=None) -> float:
+    """Mean milliseconds per call of fn on `stream`: n calls back to back
+    between two events, or (flush given) an event pair around each call with
+    the L2 flushed before it (the flush also keeps the GPU busy while the host
+    enqueues the call, so no host latency lands between the events)."""
+    if flush is None:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        b.synchronize()
+        return a.elapsed_time(b) / n
+    ev = []
+    for _ in range(n):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        ev.append((a, b))
+    ev[-1][1].synchronize()
+    return statistics.fmean(a.elapsed_time(b) for a, b in ev)
+
+
 def aggregate(t_step_ms: float, nbytes: float, dist=None, device="cpu"):
     """Whole-job figures over the ranks: the slowest rank's step time and the
     sum of every rank's bytes (host control traffic only; no data moves)."""
@@ -469,33 +501,28 @@ def run_ours(args, rank: int, world: int):
             torch.cuda.synchronize(dev)
     pkv.check()
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    # Timed region: K steps.  A batch whose KV bytes exceed the L2 several
+    # times runs its steps back to back between two events (each step reads
+    # what the previous one evicted); a smaller one flushes the L2 before every
+    # step, with an event pair around each.
+    back_to_back = kv_bytes >= 4 * L2_BYTES
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
     launches0 = pkv.launch_count()
     wall0 = time.perf_counter()
-    for i in range(args.steps):
-        # L2 flushed before every step; the flush also keeps the GPU busy while
-        # the host enqueues the step, so no host latency lands between the events
-        flush.zero_()
-        starts[i].record(stream)
-        prep.front()
-        mids[i].record(stream)
-        prep.back()
-        ends[i].record(stream)
-    torch.cuda.synchronize(dev)
+    t_step = time_loop(stream, prep, args.steps, None if back_to_back else flush)
     wall = time.perf_counter() - wall0
     if dist:
         dist.barrier()
     launches = pkv.launch_count() - launches0
     pkv.check()
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    attn_ms = [m.elapsed_time(e) for m, e in zip(mids, ends)]
-    t_step = sum(step_ms) / len(step_ms)
-    t_attn = sum(attn_ms) / len(attn_ms)
+    # the attention call alone (the step minus its copy-on-write copies), same policy
+    t_attn = time_loop(stream, prep.back, args.steps, None if back_to_back else flush)
+    # both with the L2 flushed before every step (an event pair around each)
+    t_step_fl = time_loop(stream, prep, args.steps, flush)
+    t_attn_fl = time_loop(stream, prep.back, args.steps, flush)
+    pkv.check()
 
     # paged vs contiguous placement of the same batch (identity block tables)
     nblk = -(-plan.context_lens.astype(np.int64) // w.block_size)
@@ -507,16 +534,8 @@ def run_ours(args, rank: int, world: int):
     ident_dev = torch.from_numpy(ident).to(dev)
     istep = type(step)(step.slots, step.pairs, ident_dev, step.context_lens, step.max_context_len)
     iprep = eng.prepare(q, key, value, istep, torch.empty_like(out), partition_size=P)
-    contig = []
-    for i in range(max(3, args.steps // 2)):
-        flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        iprep.attend()
-        b.record(stream)
-        contig.append((a, b))
-    torch.cuda.synchronize(dev)
-    t_contig = statistics.median([a.elapsed_time(b) for a, b in contig])
+    iprep.attend()
+    t_contig = time_loop(stream, iprep.attend, max(3, args.steps // 2), None if back_to_back else flush)
     pkv.check()
 
     # end to end through the public API from pinned host buffers: the step's inputs
@@ -584,6 +603,9 @@ def run_ours(args, rank: int, world: int):
                      "ms_per_launch": t_attn},
         "paged_overhead": {"contiguous_ms": t_contig, "paged_ms": t_attn,
                            "slowdown_pct": 100.0 * (t_attn / t_contig - 1.0)},
+        "l2_flushed_each_step": {"ms_per_step": t_step_fl, "value": kv_bytes / (t_step_fl * 1e-3) / 1e9,
+                                 "attention_ms": t_attn_fl,
+                                 "attention_gbs": kv_bytes / (t_attn_fl * 1e-3) / 1e9},
         "block_fill": frag,
         "gpu_launches": launches,
         "clocks": {**clk.summary(), "window": "warm-up + timed + e2e legs"},
