@@ -354,94 +354,98 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp == kMmaWarp) {
-        // ---------------- MMA issue (one thread) ----------------
+        // ---------------- MMA issue ----------------
         // Per item: S_0(0) S_1(0), then per key tile j: O_0 += P_0 V_j, S_0(j+1), O_1 += P_1 V_j,
         // S_1(j+1): while one tile's softmax runs, the tensor core works on the other's products.
-        // The products of one thread run in issue order, so S(j+1) overwrites P(j) only after
-        // O += P(j) V_j has read it, and the next item's first S only after this item's last
-        // product.  The next item's first O product (which overwrites O) waits for that tile's
-        // first P, which its softmax threads write only after they have read this item's O.
-        if (lane == 0) {
-            const uint32_t id_s = tc::idesc_f16(kRows, kKeys, kBf16, false);
-            // O += P V: one product of N = D per 16 keys (for D = 128 the two 64-wide panels of V
-            // are 16 KB apart, the descriptor's leading byte offset)
-            const uint32_t id_o = tc::idesc_f16(kRows, D, kBf16, true);
-            const uint32_t q_base = smem_u32(sm + L::q);
-            auto issue_s = [&](int x, int stg) {
-                const uint32_t k_base = smem_u32(sm + L::k) + (uint32_t)stg * NP * kPanelBytes;
-                const uint32_t qx = q_base + (uint32_t)x * NP * kPanelBytes;
+        // The products run in issue order, so S(j+1) overwrites P(j) only after O += P(j) V_j has
+        // read it, and the next item's first S only after this item's last product.  The next
+        // item's first O product (which overwrites O) waits for that tile's first P, which its
+        // softmax threads write only after they have read this item's O.
+        // The whole warp runs the loop (its waits and descriptors are warp-uniform values); one
+        // elected lane issues each product and commit.
+        const uint32_t id_s = tc::idesc_f16(kRows, kKeys, kBf16, false);
+        // O += P V: one product of N = D per 16 keys (for D = 128 the two 64-wide panels of V
+        // are 16 KB apart, the descriptor's leading byte offset)
+        const uint32_t id_o = tc::idesc_f16(kRows, D, kBf16, true);
+        // descriptors of the first query tile and of ring stage 0; the start-address field
+        // (address >> 4, 14 bits) takes byte offsets >> 4 without carrying out
+        const uint64_t q_desc = tc::smem_desc_sw128(smem_u32(sm + L::q), 1024, 1024);
+        const uint64_t k_desc = tc::smem_desc_sw128(smem_u32(sm + L::k), 1024, 1024);
+        const uint64_t v_desc = tc::smem_desc_sw128(smem_u32(sm + L::v), kPanelBytes, 1024);
+        constexpr uint32_t kStageStep = NP * kPanelBytes >> 4;
+        auto issue_s = [&](int x, int stg) {
+            const uint64_t kd = k_desc + (uint64_t)(stg * kStageStep);
+            const uint64_t qd = q_desc + (uint64_t)(x * kStageStep);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; kk++) {
-                    const uint32_t off = (kk / 4) * kPanelBytes + (kk % 4) * 32;
-                    tc::mma_f16_ss(tmem + x * kTileCols, tc::smem_desc_sw128(qx + off, 1024, 1024),
-                                   tc::smem_desc_sw128(k_base + off, 1024, 1024), id_s, kk > 0);
-                }
-                tc::mma_commit(&bars[bSFull + x]);
-            };
-            auto issue_o = [&](int x, int stg, bool acc) {
-                const uint32_t v_base = smem_u32(sm + L::v) + (uint32_t)stg * NP * kPanelBytes;
-                const uint32_t tp = tmem + x * kTileCols, to = tp + kKeys;
+            for (int kk = 0; kk < D / 16; kk++) {
+                const uint32_t off = ((kk / 4) * kPanelBytes + (kk % 4) * 32) >> 4;
+                tc::mma_f16_ss_warp(tmem + x * kTileCols, qd + off, kd + off, id_s, kk > 0);
+            }
+            tc::mma_commit_warp(&bars[bSFull + x]);
+        };
+        auto issue_o = [&](int x, int stg, bool acc) {
+            const uint64_t vd = v_desc + (uint64_t)(stg * kStageStep);
+            const uint32_t tp = tmem + x * kTileCols, to = tp + kKeys;
 #pragma unroll
-                for (int part = 0; part < (kBf16 ? 2 : 1); part++)
+            for (int part = 0; part < (kBf16 ? 2 : 1); part++)
 #pragma unroll
-                    for (int t = 0; t < kKeys / 16; t++)
-                        tc::mma_f16_ts(to, tp + p_col(t, part == 1),
-                                       tc::smem_desc_sw128(v_base + t * 2048, kPanelBytes, 1024), id_o,
-                                       (acc || part > 0 || t > 0) ? 1u : 0u);
-            };
-            bool ok = true;
-            int gj = 0, pc[kTiles] = {0, 0};
-            int k = 0;
-            for (;; k++) {
-                const int slot = k & 1;
-                ok = mbar_wait(&bars[bItemFull + slot], (k >> 1) & 1, kWaitLimitCycles);
-                if (!ok) break;
-                const PfItem it = items[slot];
-                mbar_arrive(&bars[bItemEmpty + slot]);
-                if (it.stop) break;
-                const int ntiles = it.rows1 ? 2 : 1, nkv = max(it.nkv0, it.nkv1);
-                ok = mbar_wait(&bars[bQFull], k & 1, kWaitLimitCycles) &&
-                     mbar_wait(&bars[bKFull + (gj & 1)], (gj >> 1) & 1, kWaitLimitCycles);
-                if (!ok) break;
-                tc::fence_after();
-                for (int x = 0; x < ntiles; x++) issue_s(x, gj & 1);
-                tc::mma_commit(&bars[bKEmpty + (gj & 1)]);
-                if (nkv == 1) tc::mma_commit(&bars[bQEmpty]);   // the item's last S has been issued
-                for (int j = 0; j < nkv && ok; j++) {
-                    const int g = gj + j, stg = g & 1;
-                    ok = mbar_wait(&bars[bVFull + stg], (g >> 1) & 1, kWaitLimitCycles);
-                    for (int x = 0; x < ntiles && ok; x++) {
-                        const int nkv_x = x ? it.nkv1 : it.nkv0;
-                        if (j >= nkv_x) continue;
-                        ok = mbar_wait(&bars[bPFull + x], pc[x] & 1, kWaitLimitCycles);
-                        pc[x]++;
+                for (int t = 0; t < kKeys / 16; t++)
+                    tc::mma_f16_ts_warp(to, tp + p_col(t, part == 1), vd + (uint64_t)(t * (2048 >> 4)), id_o,
+                                        (acc || part > 0 || t > 0) ? 1u : 0u);
+        };
+        bool ok = true;
+        int gj = 0, pc[kTiles] = {0, 0};
+        int k = 0;
+        for (;; k++) {
+            const int slot = k & 1;
+            ok = wait_warp(&bars[bItemFull + slot], (k >> 1) & 1, kWaitLimitCycles);
+            if (!ok) break;
+            const PfItem it = items[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[bItemEmpty + slot]);
+            if (it.stop) break;
+            const int ntiles = it.rows1 ? 2 : 1, nkv = max(it.nkv0, it.nkv1);
+            ok = wait_warp(&bars[bQFull], k & 1, kWaitLimitCycles) &&
+                 wait_warp(&bars[bKFull + (gj & 1)], (gj >> 1) & 1, kWaitLimitCycles);
+            if (!ok) break;
+            tc::fence_after();
+            for (int x = 0; x < ntiles; x++) issue_s(x, gj & 1);
+            tc::mma_commit_warp(&bars[bKEmpty + (gj & 1)]);
+            if (nkv == 1) tc::mma_commit_warp(&bars[bQEmpty]);   // the item's last S has been issued
+            for (int j = 0; j < nkv && ok; j++) {
+                const int g = gj + j, stg = g & 1;
+                ok = wait_warp(&bars[bVFull + stg], (g >> 1) & 1, kWaitLimitCycles);
+                for (int x = 0; x < ntiles && ok; x++) {
+                    const int nkv_x = x ? it.nkv1 : it.nkv0;
+                    if (j >= nkv_x) continue;
+                    ok = wait_warp(&bars[bPFull + x], pc[x] & 1, kWaitLimitCycles);
+                    pc[x]++;
+                    if (!ok) break;
+                    tc::fence_after();
+                    issue_o(x, stg, j > 0);
+                    if (j + 1 == nkv_x) {
+                        tc::mma_commit_warp(&bars[bODone + x]);
+                    } else {
+                        ok = wait_warp(&bars[bKFull + ((g + 1) & 1)], ((g + 1) >> 1) & 1, kWaitLimitCycles);
                         if (!ok) break;
                         tc::fence_after();
-                        issue_o(x, stg, j > 0);
-                        if (j + 1 == nkv_x) {
-                            tc::mma_commit(&bars[bODone + x]);
-                        } else {
-                            ok = mbar_wait(&bars[bKFull + ((g + 1) & 1)], ((g + 1) >> 1) & 1, kWaitLimitCycles);
-                            if (!ok) break;
-                            tc::fence_after();
-                            issue_s(x, (g + 1) & 1);
-                        }
-                    }
-                    if (ok) {
-                        tc::mma_commit(&bars[bVEmpty + stg]);                        // V_j read by every tile
-                        if (j + 1 < nkv) tc::mma_commit(&bars[bKEmpty + ((g + 1) & 1)]);   // K_{j+1} too
-                        if (j + 2 == nkv) tc::mma_commit(&bars[bQEmpty]);            // and the last S issued
+                        issue_s(x, (g + 1) & 1);
                     }
                 }
-                if (!ok) break;
-                gj += nkv;
+                if (ok) {
+                    tc::mma_commit_warp(&bars[bVEmpty + stg]);                        // V_j read by every tile
+                    if (j + 1 < nkv) tc::mma_commit_warp(&bars[bKEmpty + ((g + 1) & 1)]);   // K_{j+1} too
+                    if (j + 2 == nkv) tc::mma_commit_warp(&bars[bQEmpty]);            // and the last S issued
+                }
             }
-            if (!ok) latch(st, kFlagTimeout, 1000000 + k);
-            // every MMA issued so far, and every arrive it makes, completes before the CTA
-            // frees its TMEM and shared memory
-            tc::mma_commit(&bars[bDrain]);
-            mbar_wait(&bars[bDrain], 0, ok ? kWaitLimitCycles : kDrainLimitCycles);
+            if (!ok) break;
+            gj += nkv;
         }
+        if (!ok && lane == 0) latch(st, kFlagTimeout, 1000000 + k);
+        // every MMA issued so far, and every arrive it makes, completes before the CTA
+        // frees its TMEM and shared memory
+        tc::mma_commit_warp(&bars[bDrain]);
+        wait_warp(&bars[bDrain], 0, ok ? kWaitLimitCycles : kDrainLimitCycles);
         __syncwarp();
     } else {
         // ---------------- softmax: one thread per query row of its tile ----------------
