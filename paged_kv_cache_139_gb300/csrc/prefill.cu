@@ -55,9 +55,10 @@ constexpr int kTiles = 2;                // query tiles per CTA, alternating on 
 constexpr int kKeys = 128;               // keys per KV tile
 constexpr int kStages = 2;               // K/V ring depth
 constexpr int kSoftmaxWarps = 4;         // per query tile
-constexpr int kProducerWarp = kTiles * kSoftmaxWarps;
+constexpr int kProducerWarp = kTiles * kSoftmaxWarps;   // items, queries, keys
 constexpr int kMmaWarp = kProducerWarp + 1;
-constexpr int kThreads = (kMmaWarp + 1) * 32;
+constexpr int kValueWarp = kMmaWarp + 1;                // values
+constexpr int kThreads = (kValueWarp + 1) * 32;
 constexpr uint32_t kPanelBytes = 128 * 128;   // 128 rows x 64 16-bit elements
 constexpr uint32_t kTmemCols = 512;           // per tile: S/P 128 columns, O 128
 constexpr uint32_t kTileCols = 256;
@@ -106,8 +107,8 @@ template <int D> struct PfLayout {
 // barrier slots
 enum : int { bQFull = 0, bQEmpty = 1, bKFull = 2, bVFull = 4, bKEmpty = 6, bVEmpty = 8, bSFull = 10, bPFull = 12,
              bODone = 14, bItemFull = 16, bItemEmpty = 18, bDrain = 20, kNumBars = 21 };
-// an item slot is released by every softmax warp and the MMA warp
-constexpr int kItemReaders = kTiles * kSoftmaxWarps + 1;
+// an item slot is released by every softmax warp, the MMA warp and the value warp
+constexpr int kItemReaders = kTiles * kSoftmaxWarps + 2;
 
 // 2^x by the hardware approximation (MUFU); 2^-inf = 0.
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -311,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     phys = 0;                                   // keep the byte count; the output is flagged
                 }
                 const uint32_t bytes = (uint32_t)nb * (uint32_t)B * 128u * NP;
-                for (int which = 0; which < 2; which++) {       // K, then V
+                for (int which = 0; which < 1; which++) {       // K (the value warp loads V)
                     if (gj >= kStages) {
                         ok = wait_warp(&bars[(which ? bVEmpty : bKEmpty) + stg], ((gj >> 1) - 1) & 1,
                                        kWaitLimitCycles);
@@ -338,10 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) {
             if (lane == 0) latch(st, kFlagTimeout, gj);
             // copies already issued must land before the CTA's memory is reused
-            for (int jj = max(0, gj - kStages); jj <= gj; jj++) {
+            for (int jj = max(0, gj - kStages); jj <= gj; jj++)
                 mbar_wait(&bars[bKFull + (jj & 1)], (jj >> 1) & 1, kDrainLimitCycles);
-                mbar_wait(&bars[bVFull + (jj & 1)], (jj >> 1) & 1, kDrainLimitCycles);
-            }
             mbar_wait(&bars[bQFull], k & 1, kDrainLimitCycles);
         }
         // the last CTA to finish leaves the counters at zero for the next call
@@ -352,6 +351,58 @@ __global__ void __launch_bounds__(kThreads, 1)
                 hdr->done = 0;
                 __threadfence();
             }
+        }
+    } else if (warp == kValueWarp) {
+        // ---------------- values: per item, its V tiles into their own two-stage ring ----------------
+        // A warp of its own, so that the values' copies are issued beside the keys', not
+        // behind them (each tile takes its issuing warp about half a microsecond at B = 16).
+        const uint64_t pol_kv = policy_evict_last();
+        bool ok = true;
+        int gj = 0, k = 0;
+        for (;; k++) {
+            const int slot = k & 1;
+            ok = wait_warp(&bars[bItemFull + slot], (k >> 1) & 1, kWaitLimitCycles);
+            if (!ok) break;
+            const PfItem it = items[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[bItemEmpty + slot]);
+            if (it.stop) break;
+            const int nkv = max(it.nkv0, it.nkv1);
+            const int g = it.h / a.group;
+            const int32_t *row = a.block_tables + (size_t)it.s * a.max_blocks;
+            const int nblk_used = (it.ctx + B - 1) >> a.log2_block;
+            const int bpt = kKeys >> a.log2_block;
+            auto blocks_in = [&](int jj) { return min(bpt, nblk_used - jj * bpt); };
+            int cb = lane < blocks_in(0) ? row[lane] : 0;
+            for (int j = 0; j < nkv; j++, gj++) {
+                const int stg = gj & 1;
+                const int nb = blocks_in(j);
+                const int nxt = (j + 1 < nkv && lane < blocks_in(j + 1)) ? row[(j + 1) * bpt + lane] : 0;
+                int phys = cb;
+                if (lane < nb && (phys < 0 || phys >= a.num_blocks)) {
+                    latch(st, kFlagBadBlock, phys);
+                    phys = 0;
+                }
+                if (gj >= kStages) {
+                    ok = wait_warp(&bars[bVEmpty + stg], ((gj >> 1) - 1) & 1, kWaitLimitCycles);
+                    if (!ok) break;
+                }
+                uint64_t *full = &bars[bVFull + stg];
+                if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)nb * (uint32_t)B * 128u * NP);
+                __syncwarp();
+                uint8_t *dst = sm + L::v + (uint32_t)stg * NP * kPanelBytes;
+                if (lane < nb)
+                    for (int p = 0; p < NP; p++)
+                        tma_load_4d(dst + p * kPanelBytes + (uint32_t)lane * B * 128u, &tmv, 64 * p, 0, g, phys, full,
+                                    pol_kv);
+                cb = nxt;
+            }
+            if (!ok) break;
+        }
+        if (!ok) {
+            if (lane == 0) latch(st, kFlagTimeout, 3000000 + gj);
+            for (int jj = max(0, gj - kStages); jj <= gj; jj++)
+                mbar_wait(&bars[bVFull + (jj & 1)], (jj >> 1) & 1, kDrainLimitCycles);
         }
     } else if (warp == kMmaWarp) {
         // ---------------- MMA issue ----------------
