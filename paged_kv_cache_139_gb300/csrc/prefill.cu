@@ -85,7 +85,8 @@ struct PfItem {
     int rows0, rows1;                    // valid rows of the two tiles (rows1 = 0: one tile)
     int nkv0, nkv1;                      // key tiles each tile reads
     int stop;                            // no further items
-    int pad[5];
+    int split;                           // one query tile, its key tiles alternating between both slots
+    int pad[4];
 };
 
 // Shared memory: the two query tiles, the K/V ring, two item slots and a
@@ -106,7 +107,7 @@ template <int D> struct PfLayout {
 
 // barrier slots
 enum : int { bQFull = 0, bQEmpty = 1, bKFull = 2, bVFull = 4, bKEmpty = 6, bVEmpty = 8, bSFull = 10, bPFull = 12,
-             bODone = 14, bItemFull = 16, bItemEmpty = 18, bDrain = 20, kNumBars = 21 };
+             bODone = 14, bItemFull = 16, bItemEmpty = 18, bDrain = 20, bMerge = 21, bMerged = 22, kNumBars = 23 };
 // an item slot is released by every softmax warp, the MMA warp and the value warp
 constexpr int kItemReaders = kTiles * kSoftmaxWarps + 2;
 
@@ -216,6 +217,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars[bItemEmpty + i], kItemReaders);
         }
         mbar_init(&bars[bDrain], 1);
+        mbar_init(&bars[bMerge], kSoftmaxWarps * 32);
+        mbar_init(&bars[bMerged], kSoftmaxWarps * 32);
         fence_mbar_init();
     }
     if (warp == kMmaWarp) tc::tmem_alloc(tslot, kTmemCols);
@@ -257,6 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     o.nkv0 = (o.pos00 + o.rows0 - 1) / kKeys + 1;
                     o.nkv1 = o.rows1 ? (o.pos00 + kRows + o.rows1 - 1) / kKeys + 1 : 0;
                     o.stop = 0;
+                    o.split = (o.rows1 == 0 && o.nkv0 >= 2) ? 1 : 0;
                     return t;
                 }
                 t = next_ticket(t);
@@ -424,9 +428,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t k_desc = tc::smem_desc_sw128(smem_u32(sm + L::k), 1024, 1024);
         const uint64_t v_desc = tc::smem_desc_sw128(smem_u32(sm + L::v), kPanelBytes, 1024);
         constexpr uint32_t kStageStep = NP * kPanelBytes >> 4;
-        auto issue_s = [&](int x, int stg) {
+        // S of slot x (its TMEM columns) from query buffer qx
+        auto issue_s = [&](int x, int stg, int qx) {
             const uint64_t kd = k_desc + (uint64_t)(stg * kStageStep);
-            const uint64_t qd = q_desc + (uint64_t)(x * kStageStep);
+            const uint64_t qd = q_desc + (uint64_t)(qx * kStageStep);
 #pragma unroll
             for (int kk = 0; kk < D / 16; kk++) {
                 const uint32_t off = ((kk / 4) * kPanelBytes + (kk % 4) * 32) >> 4;
@@ -460,7 +465,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                  wait_warp(&bars[bKFull + (gj & 1)], (gj >> 1) & 1, kWaitLimitCycles);
             if (!ok) break;
             tc::fence_after();
-            for (int x = 0; x < ntiles; x++) issue_s(x, gj & 1);
+            if (it.split) {
+                // One query tile; key tile j goes to slot j % 2, each slot with its own S, P and O:
+                // S_0(0) S_1(1), then per key tile j: O_x += P_x V_j, S_x(j + 2).  The slots'
+                // softmax chains overlap as the two tiles' do in a pair.
+                issue_s(0, gj & 1, 0);
+                tc::mma_commit_warp(&bars[bKEmpty + (gj & 1)]);
+                ok = wait_warp(&bars[bKFull + ((gj + 1) & 1)], ((gj + 1) >> 1) & 1, kWaitLimitCycles);
+                if (!ok) break;
+                tc::fence_after();
+                issue_s(1, (gj + 1) & 1, 0);
+                tc::mma_commit_warp(&bars[bKEmpty + ((gj + 1) & 1)]);
+                if (nkv == 2) tc::mma_commit_warp(&bars[bQEmpty]);
+                for (int j = 0; j < nkv && ok; j++) {
+                    const int g = gj + j, stg = g & 1, x = j & 1;
+                    const int pcx = x ? pc[1] : pc[0];          // (no dynamic index: pc stays in registers)
+                    ok = wait_warp(&bars[bVFull + stg], (g >> 1) & 1, kWaitLimitCycles) &&
+                         wait_warp(&bars[bPFull + x], pcx & 1, kWaitLimitCycles);
+                    if (x) pc[1]++;
+                    else pc[0]++;
+                    if (!ok) break;
+                    tc::fence_after();
+                    issue_o(x, stg, j >= 2);
+                    if (j + 2 < nkv) {
+                        ok = wait_warp(&bars[bKFull + ((g + 2) & 1)], ((g + 2) >> 1) & 1, kWaitLimitCycles);
+                        if (!ok) break;
+                        tc::fence_after();
+                        issue_s(x, (g + 2) & 1, 0);
+                        tc::mma_commit_warp(&bars[bKEmpty + ((g + 2) & 1)]);      // K_{j+2} read
+                        if (j + 3 == nkv) tc::mma_commit_warp(&bars[bQEmpty]);  // the item's last S
+                    } else {
+                        tc::mma_commit_warp(&bars[bODone + x]);
+                    }
+                    tc::mma_commit_warp(&bars[bVEmpty + stg]);                    // V_j read
+                }
+                if (!ok) break;
+                gj += nkv;
+                continue;
+            }
+            for (int x = 0; x < ntiles; x++) issue_s(x, gj & 1, x);
             tc::mma_commit_warp(&bars[bKEmpty + (gj & 1)]);
             if (nkv == 1) tc::mma_commit_warp(&bars[bQEmpty]);   // the item's last S has been issued
             for (int j = 0; j < nkv && ok; j++) {
@@ -480,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = wait_warp(&bars[bKFull + ((g + 1) & 1)], ((g + 1) >> 1) & 1, kWaitLimitCycles);
                         if (!ok) break;
                         tc::fence_after();
-                        issue_s(x, (g + 1) & 1);
+                        issue_s(x, (g + 1) & 1, x);
                     }
                 }
                 if (ok) {
@@ -505,7 +548,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = (uint32_t)(32 * (warp % 4)) << 16;
         const uint32_t tS = tmem + x * kTileCols + lane_off, tO = tS + kKeys;
         bool ok = true;
-        int gj = 0, sc = 0, u = 0, k = 0, j = 0;
+        int gj = 0, sc = 0, u = 0, k = 0, j = 0, um = 0;
+        // split items: the other slot's O and the buffer for its (max, sum)
+        const uint32_t tO1 = tmem + kTileCols + lane_off + kKeys;
+        float *xch = reinterpret_cast<float *>(sm + L::stage + (uint32_t)(kSoftmaxWarps + warp % 4) * 4096u);
         for (;; k++) {
             const int slot = k & 1;
             ok = wait_warp(&bars[bItemFull + slot], (k >> 1) & 1, kWaitLimitCycles);
@@ -517,14 +563,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nkv = max(it.nkv0, it.nkv1);
             const int gbase = gj;
             gj += nkv;
-            const int rows_x = x ? it.rows1 : it.rows0;
+            const bool split = it.split != 0;
+            // split: both slots serve tile 0's rows, slot x its key tiles x, x + 2, ...
+            const int rows_x = split ? it.rows0 : (x ? it.rows1 : it.rows0);
             if (rows_x <= 0) continue;
-            const int pos0_x = it.pos00 + x * kRows, nkv_x = x ? it.nkv1 : it.nkv0;
+            const int pos0_x = split ? it.pos00 : it.pos00 + x * kRows;
+            const int nkv_x = split ? (nkv - x + 1) / 2 : (x ? it.nkv1 : it.nkv0);
+            const int kstep = split ? 2 : 1, kfirst = split ? x : 0;
             const int my_pos = r < rows_x ? pos0_x + r : pos0_x + rows_x - 1;   // last key this row sees
             float m_run = -INFINITY, l_run = 0.f;
-            // the tile that zeroes V rows past the context (before its product reads them)
-            const bool zero_duty = (x == 0) == (it.nkv0 == nkv);
-            for (j = 0; j < nkv_x; j++) {
+            // the slot that zeroes V rows past the context (before its product reads them)
+            const bool zero_duty = split ? x == ((nkv - 1) & 1) : (x == 0) == (it.nkv0 == nkv);
+            for (int i = 0; i < nkv_x; i++) {
+                j = kfirst + kstep * i;                      // the key tile
                 ok = wait_warp(&bars[bSFull + x], sc & 1, kWaitLimitCycles);
                 sc++;
                 if (!ok) break;
@@ -566,10 +617,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float mx = mraw * c2;                   // -inf when no key of the tile is visible
                 const bool moved = mx > m_run + kRescaleLog2;
                 const float m_new = moved ? mx : m_run;
-                const float alpha = fast_exp2(m_run - m_new);  // 0 on the first tile, 1 when not moved
+                // 0 on the first visible tile, 1 when not moved (and while no key was visible)
+                const float alpha = m_new == -INFINITY ? 1.f : fast_exp2(m_run - m_new);
                 m_run = m_new;
                 // O of the previous tiles is complete (its products were issued before this S)
-                if (j > 0 && __any_sync(0xffffffffu, moved)) {
+                if (i > 0 && __any_sync(0xffffffffu, moved)) {
 #pragma unroll
                     for (int c = 0; c < D / 32; c++) {
                         uint32_t o[32];
@@ -638,7 +690,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             u++;
             if (!ok) break;
             tc::fence_after();
+            float a0 = 1.f, a1 = 0.f;                        // weights of this slot's O and the other's
+            if (split) {
+                if (x == 1) {
+                    // hand (max, sum) to slot 0, which merges; wait until it has read this O
+                    xch[2 * lane] = m_run;
+                    xch[2 * lane + 1] = l_run;
+                    tc::fence_before();
+                    mbar_arrive(&bars[bMerge]);
+                    ok = wait_warp(&bars[bMerged], um & 1, kWaitLimitCycles);
+                    um++;
+                    if (!ok) break;
+                    continue;
+                }
+                ok = wait_warp(&bars[bMerge], um & 1, kWaitLimitCycles);
+                if (!ok) break;
+                tc::fence_after();
+                const float m1 = xch[2 * lane], l1 = xch[2 * lane + 1];
+                const float M = fmaxf(m_run, m1);
+                a0 = fast_exp2(m_run - M);
+                a1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M);
+                l_run = l_run * a0 + l1 * a1;
+            }
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            // 32 columns of this row's output (over both slots of a split item), unscaled
+            auto load_out = [&](int col, uint32_t (&o)[32]) {
+                tc::tmem_ld32(tO + col, o);
+                if (split) {
+                    uint32_t o1[32];
+                    tc::tmem_ld32(tO1 + col, o1);
+                    tc::tmem_wait_ld(o);
+                    tc::tmem_wait_ld(o1);
+#pragma unroll
+                    for (int i = 0; i < 32; i++)
+                        o[i] = __float_as_uint(fmaf(__uint_as_float(o[i]), a0, __uint_as_float(o1[i]) * a1));
+                } else {
+                    tc::tmem_wait_ld(o);
+                }
+            };
             // Each 64-column panel of the warp's 32 rows goes through the warp's buffer: every
             // thread writes its row (16-byte units swizzled by row, free of bank conflicts), then
             // each store instruction writes 4 whole 128-byte row segments.
@@ -651,8 +740,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < 2; c++) {
                     uint32_t o[32];
-                    tc::tmem_ld32(tO + 64 * p + 32 * c, o);
-                    tc::tmem_wait_ld(o);
+                    load_out(64 * p + 32 * c, o);
 #pragma unroll
                     for (int v = 0; v < 4; v++) {
                         uint4 w;
@@ -673,6 +761,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (trow < rows_x) *reinterpret_cast<uint4 *>(obase + (size_t)trow * rstride + 64 * p + 8 * unit) = w;
                 }
                 __syncwarp();
+            }
+            if (split) {
+                // the other slot's O has been read: its softmax threads may go on
+                tc::fence_before();
+                mbar_arrive(&bars[bMerged]);
+                um++;
             }
         }
         if (!ok && lane == 0) latch(st, kFlagTimeout, 2000000 + 1000 * k + j);
