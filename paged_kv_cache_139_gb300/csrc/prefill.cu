@@ -20,14 +20,20 @@
 //   * A producer warp claims and looks up the next item while the current one
 //     streams and hands it to the other warps through a two-slot item ring; it
 //     loads each item's query tiles (tiled TMA over the query tensor) and then,
-//     for each 128-key tile, the tile's K and V blocks (tiled TMA over the
-//     cache, one box of B tokens x 64 elements per block and 64-element panel
-//     of d) into a two-stage ring that runs on across items.  Boxes land
-//     128-byte swizzled, the layout the MMA descriptors describe.
-//   * One thread of the MMA warp issues tcgen05.mma: S = Q K^T (M 128, N 128,
-//     fp32 in TMEM), then O += P V with P read from TMEM and V read MN-major
-//     straight from the cache layout (N = d: one product per 16 keys).  While one tile's
-//     softmax runs, the tensor core computes the other tile's products.
+//     for each 128-key tile, the tile's K blocks (tiled TMA over the cache, one
+//     box of B tokens x 64 elements per block and 64-element panel of d) into
+//     a two-stage ring that runs on across items; a value warp does the same
+//     for the V blocks in a ring of its own, so that neither waits behind the
+//     other's copy issue.  Boxes land 128-byte swizzled, the layout the MMA
+//     descriptors describe.
+//   * The MMA warp (converged; one elected lane issues) runs tcgen05.mma:
+//     S = Q K^T (M 128, N 128, fp32 in TMEM), then O += P V with P read from
+//     TMEM and V read MN-major straight from the cache layout (N = d: one
+//     product per 16 keys).  While one tile's softmax runs, the tensor core
+//     computes the other tile's products.  An item with a single query tile
+//     gives its key tiles alternately to both tiles' TMEM and softmax warps
+//     (each pair of key tiles then overlaps as the two tiles of a pair do),
+//     and the two partial outputs are merged at the end.
 //   * Four softmax warps per tile (one thread per row) read S from TMEM, mask
 //     keys after the row's position, keep a running max and sum in fp32 (log2
 //     domain; the reference max moves only when it grows by more than 8, so
