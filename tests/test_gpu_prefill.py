@@ -273,3 +273,25 @@ def test_one_tile_items_split_over_both_groups(cuda_device, dtype, H, Hkv):
     ctx = (200, 259, 484, 1000, 130, 900)
     new = (128, 5, 50, 1, 2, 300)
     _check(PrefillCase(custom(ctx, new, H=H, Hkv=Hkv, dtype=dtype), cuda_device), f"split items {dtype}")
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_seeded_random_batches(cuda_device, seed):
+    """Seeded random prompt-phase batches: 1-7 sequences, 0-600 new tokens
+    after 0-1500 cached ones, head dim 64 or 128, block size 4-128, MHA or
+    grouped heads, fp16 or bf16 -- pair, split and one-key-tile items mixed in
+    one launch, against the oracle."""
+    rng = np.random.default_rng(9000 + seed)
+    S = int(rng.integers(1, 8))
+    new = rng.integers(0, 601, size=S)
+    ctx = new + rng.integers(0, 1501, size=S)
+    ctx = np.maximum(ctx, 1)
+    new = np.minimum(new, ctx)
+    d = int(rng.choice([64, 128]))
+    B = int(rng.choice([4, 8, 16, 32, 64, 128]))
+    Hkv = int(rng.choice([1, 2, 4]))
+    H = Hkv * int(rng.choice([1, 2, 4]))
+    dtype = str(rng.choice(["f16", "bf16"]))
+    w = custom(tuple(int(c) for c in ctx), tuple(int(n) for n in new), H=H, Hkv=Hkv, d=d, B=B, dtype=dtype,
+               seed=700 + seed)
+    _check(PrefillCase(w, cuda_device), f"random batch {seed}: S={S} d={d} B={B} H={H}/{Hkv} {dtype}")
