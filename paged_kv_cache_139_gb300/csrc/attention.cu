@@ -1352,8 +1352,13 @@ int current_dev() {
     return cudaGetDevice(&d) == cudaSuccess ? d : -1;
 }
 
+// Workspaces remembered at most; past that the record starts afresh, and a
+// workspace it has forgotten gets its counters zeroed once more (never wrong).
+constexpr size_t kMaxRememberedWorkspaces = 4096;
+
 void ws_remember(const void *ws, const WsSig &sig) {
     std::lock_guard<std::mutex> lk(g_ws_mu);
+    if (g_ws_last.size() >= kMaxRememberedWorkspaces) g_ws_last.clear();
     g_ws_last[{current_dev(), reinterpret_cast<uintptr_t>(ws)}] = sig;
 }
 
