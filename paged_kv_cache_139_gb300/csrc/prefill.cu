@@ -79,20 +79,25 @@ struct PrefillArgs {
     WsHeader *hdr;                       // ticket counters; null: static round robin
     int num_seqs, num_tokens, max_blocks, log2_block, num_blocks;
     int num_heads, group;
-    int num_pairs;                       // 256-row tiles pairs per sequence (of the longest)
-    int num_items;                       // num_pairs x num_heads x num_seqs tickets
+    int head_pairs;                      // 1: an item's two tiles are the same rows of two query heads
+                                         // of one kv head (group even); 0: two row tiles of one head
+    int num_pairs;                       // row tiles (head_pairs) or pairs of them per sequence (of the longest)
+    int num_items;                       // num_pairs x (query heads, or head pairs) x num_seqs tickets
     float scale_log2;                    // scale * log2(e)
 };
 
 // A work item as the producer publishes it to the other warps: (sequence s,
-// query head h, the two 128-row tiles from new token t0).
+// query head h, the two 128-row tiles from new token t0), or (sequence s,
+// query heads h and h1 of one kv head, the 128-row tile from t0 of each).
 struct PfItem {
     int s, h, t0, q_begin, ctx, pos00;   // pos00: position of the item's first new token
     int rows0, rows1;                    // valid rows of the two tiles (rows1 = 0: one tile)
     int nkv0, nkv1;                      // key tiles each tile reads
     int stop;                            // no further items
     int split;                           // one query tile, its key tiles alternating between both slots
-    int pad[4];
+    int h1;                              // query head of tile 1
+    int rstep;                           // rows between the tiles' first tokens: 128, or 0 (two heads)
+    int pad[2];
 };
 
 // Shared memory: the two query tiles, the K/V ring, two item slots and a
@@ -158,14 +163,16 @@ template <> __device__ __forceinline__ uint32_t pack16<__nv_bfloat16>(float x, f
 // fp16 (11 bits) needs one.
 __device__ __forceinline__ uint32_t p_col(int t, bool lo) { return 32 * (t >> 1) + 8 * (t & 1) + (lo ? 16 : 0); }
 
-// Ticket t in [0, num_items): the longest pairs of tiles first (pair index
-// descending), then sequence, then head.
+// Ticket t in [0, num_items): the tiles with the most keys first (row-tile or
+// pair index descending), then sequence, then head (or head pair: h is its
+// first head).
 __device__ __forceinline__ void ticket_item(const PrefillArgs &a, int t, int &s, int &h, int &pair) {
-    const int hs = a.num_heads * a.num_seqs;
+    const int nh = a.head_pairs ? a.num_heads / 2 : a.num_heads;
+    const int hs = nh * a.num_seqs;
     pair = a.num_pairs - 1 - t / hs;
     const int rem = t % hs;
-    s = rem / a.num_heads;
-    h = rem % a.num_heads;
+    s = rem / nh;
+    h = (rem % nh) * (a.head_pairs ? 2 : 1);
 }
 
 template <int D, typename T>
@@ -251,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int s, h, pair;
                 ticket_item(a, t, s, h, pair);
                 const int qb = a.query_start[s], qe = a.query_start[s + 1], ctx = a.context_lens[s];
-                const int n = qe - qb, t0 = pair * kTiles * kRows;
+                const int n = qe - qb, t0 = pair * (a.head_pairs ? kRows : kTiles * kRows);
                 if (n < 0 || qb < 0 || qe > a.num_tokens || n > ctx || ctx > a.max_blocks * B) {
                     if (lane == 0 && pair == 0 && h == 0) latch(st, kFlagBadContext, s);
                 } else if (t0 < n) {
@@ -262,9 +269,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     o.ctx = ctx;
                     o.pos00 = ctx - n + t0;
                     o.rows0 = min(kRows, n - t0);
-                    o.rows1 = max(0, min(kRows, n - t0 - kRows));
                     o.nkv0 = (o.pos00 + o.rows0 - 1) / kKeys + 1;
-                    o.nkv1 = o.rows1 ? (o.pos00 + kRows + o.rows1 - 1) / kKeys + 1 : 0;
+                    if (a.head_pairs) {                        // the same rows of the next head
+                        o.rows1 = o.rows0;
+                        o.nkv1 = o.nkv0;
+                        o.h1 = h + 1;
+                        o.rstep = 0;
+                    } else {
+                        o.rows1 = max(0, min(kRows, n - t0 - kRows));
+                        o.nkv1 = o.rows1 ? (o.pos00 + kRows + o.rows1 - 1) / kKeys + 1 : 0;
+                        o.h1 = h;
+                        o.rstep = kRows;
+                    }
                     o.stop = 0;
                     o.split = (o.rows1 == 0 && o.nkv0 >= 2) ? 1 : 0;
                     return t;
@@ -301,8 +317,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(&bars[bQFull], ntiles * NP * kPanelBytes);
                 for (int x = 0; x < ntiles; x++)
                     for (int p = 0; p < NP; p++)
-                        tma_load_3d(sm + L::q + (x * NP + p) * kPanelBytes, &tmq, 64 * p, cur.h,
-                                    cur.q_begin + cur.t0 + x * kRows, &bars[bQFull], pol_q);
+                        tma_load_3d(sm + L::q + (x * NP + p) * kPanelBytes, &tmq, 64 * p, x ? cur.h1 : cur.h,
+                                    cur.q_begin + cur.t0 + x * cur.rstep, &bars[bQFull], pol_q);
             }
             const int32_t *row = a.block_tables + (size_t)cur.s * a.max_blocks;
             const int nblk_used = (cur.ctx + B - 1) >> a.log2_block;
@@ -573,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // split: both slots serve tile 0's rows, slot x its key tiles x, x + 2, ...
             const int rows_x = split ? it.rows0 : (x ? it.rows1 : it.rows0);
             if (rows_x <= 0) continue;
-            const int pos0_x = split ? it.pos00 : it.pos00 + x * kRows;
+            const int pos0_x = split ? it.pos00 : it.pos00 + x * it.rstep;
             const int nkv_x = split ? (nkv - x + 1) / 2 : (x ? it.nkv1 : it.nkv0);
             const int kstep = split ? 2 : 1, kfirst = split ? x : 0;
             const int my_pos = r < rows_x ? pos0_x + r : pos0_x + rows_x - 1;   // last key this row sees
@@ -739,7 +755,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // each store instruction writes 4 whole 128-byte row segments.
             uint8_t *wb = sm + L::stage + (uint32_t)warp * 4096u;
             const int wrow0 = 32 * (warp % 4);              // the warp's first tile row
-            T *obase = reinterpret_cast<T *>(a.out) + ((size_t)(it.q_begin + it.t0 + x * kRows) * a.num_heads + it.h) * D;
+            T *obase = reinterpret_cast<T *>(a.out) +
+                       ((size_t)(it.q_begin + it.t0 + x * it.rstep) * a.num_heads + (x ? it.h1 : it.h)) * D;
             const size_t rstride = (size_t)a.num_heads * D;
 #pragma unroll
             for (int p = 0; p < NP; p++) {
@@ -860,9 +877,12 @@ extern "C" pkv_status paged_attention_prefill(void *out, const void *query, cons
     if (workspace && (!aligned16(workspace) || workspace_bytes < kWsHeaderBytes))
         return fail(PKV_EINVAL, "paged_attention_prefill: workspace must be 16-byte aligned and at least %zu bytes",
                     kWsHeaderBytes);
-    const int rows_per_pair = kTiles * kRows;
-    const long long num_pairs = ((long long)max_query_len + rows_per_pair - 1) / rows_per_pair;
-    const long long num_items = num_pairs * num_heads * num_seqs;
+    // grouped query heads share their kv head's tiles: pair the heads, not the rows
+    const int group = num_heads / num_kv_heads;
+    const bool head_pairs = group % 2 == 0;
+    const int rows_per_item = head_pairs ? kRows : kTiles * kRows;
+    const long long num_pairs = ((long long)max_query_len + rows_per_item - 1) / rows_per_item;
+    const long long num_items = num_pairs * (head_pairs ? num_heads / 2 : num_heads) * num_seqs;
     if (num_items > INT_MAX / 2)
         return fail(PKV_EINVAL, "paged_attention_prefill: %lld work items (query tile pairs x heads x sequences) "
                                 "above 2^30", num_items);
@@ -876,6 +896,7 @@ extern "C" pkv_status paged_attention_prefill(void *out, const void *query, cons
     a.status = st;
     a.hdr = reinterpret_cast<WsHeader *>(workspace);
     a.num_pairs = (int)num_pairs;
+    a.head_pairs = head_pairs ? 1 : 0;
     a.num_items = (int)num_items;
     a.num_seqs = num_seqs;
     a.num_tokens = num_tokens;
