@@ -233,7 +233,9 @@ pkv_status paged_attention_decode_noalloc(void *out_dev, const void *query_dev,
  *   workspace_dev       NULL, or at least 256 bytes prepared once by
  *                       paged_attention_workspace_init (a decode workspace
  *                       serves as well).  The work -- pairs of 128-row query
- *                       tiles of one (sequence, head) -- is spread over one
+ *                       tiles of one (sequence, head), or with an even number
+ *                       of query heads per kv head the same 128 rows of two
+ *                       query heads that share a kv head -- is spread over one
  *                       CTA per SM; with a workspace the CTAs take items from
  *                       a counter in it (balanced), without one each takes a
  *                       fixed share (round robin).  The call leaves the
@@ -243,8 +245,9 @@ pkv_status paged_attention_decode_noalloc(void *out_dev, const void *query_dev,
  *                       (pkv_check) and computes nothing.
  * The call allocates nothing.  num_seqs <= 65535; head_dim in {64, 128};
  * block_size a power of two in [4, 128]; num_heads % num_kv_heads == 0;
- * scale > 0 (usually 1/sqrt(head_dim)); ceil(max_query_len / 256) x
- * num_heads x num_seqs <= 2^30.  Asynchronous on `stream`; PKV_EINVAL for
+ * scale > 0 (usually 1/sqrt(head_dim)); the work items (ceil(max_query_len /
+ * 256) x num_heads x num_seqs, or ceil(max_query_len / 128) x num_heads / 2 x
+ * num_seqs for paired heads) <= 2^30.  Asynchronous on `stream`; PKV_EINVAL for
  * bad arguments, launching nothing.
  * ------------------------------------------------------------------------- */
 pkv_status paged_attention_prefill(void *out_dev, const void *query_dev,
