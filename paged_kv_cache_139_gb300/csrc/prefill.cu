@@ -440,10 +440,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // softmax threads write only after they have read this item's O.
         // The whole warp runs the loop (its waits and descriptors are warp-uniform values); one
         // elected lane issues each product and commit.
-        const uint32_t id_s = tc::idesc_f16(kRows, kKeys, kBf16, false);
+        // A tile of 64 rows or fewer takes M = 64 products (half the tensor work); their rows
+        // sit in TMEM lanes 0-15 of each 32-lane quarter (row r in lane 32 (r / 16) + r % 16).
+        const uint32_t id_s128 = tc::idesc_f16(kRows, kKeys, kBf16, false), id_s64 = tc::idesc_f16(64, kKeys, kBf16, false);
         // O += P V: one product of N = D per 16 keys (for D = 128 the two 64-wide panels of V
         // are 16 KB apart, the descriptor's leading byte offset)
-        const uint32_t id_o = tc::idesc_f16(kRows, D, kBf16, true);
+        const uint32_t id_o128 = tc::idesc_f16(kRows, D, kBf16, true), id_o64 = tc::idesc_f16(64, D, kBf16, true);
+        int m64m = 0;                                    // bit x: slot x of the current item has M = 64
         // descriptors of the first query tile and of ring stage 0; the start-address field
         // (address >> 4, 14 bits) takes byte offsets >> 4 without carrying out
         const uint64_t q_desc = tc::smem_desc_sw128(smem_u32(sm + L::q), 1024, 1024);
@@ -457,7 +460,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < D / 16; kk++) {
                 const uint32_t off = ((kk / 4) * kPanelBytes + (kk % 4) * 32) >> 4;
-                tc::mma_f16_ss_warp(tmem + x * kTileCols, qd + off, kd + off, id_s, kk > 0);
+                tc::mma_f16_ss_warp(tmem + x * kTileCols, qd + off, kd + off, (m64m >> x) & 1 ? id_s64 : id_s128,
+                                    kk > 0);
             }
             tc::mma_commit_warp(&bars[bSFull + x]);
         };
@@ -468,8 +472,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int part = 0; part < (kBf16 ? 2 : 1); part++)
 #pragma unroll
                 for (int t = 0; t < kKeys / 16; t++)
-                    tc::mma_f16_ts_warp(to, tp + p_col(t, part == 1), vd + (uint64_t)(t * (2048 >> 4)), id_o,
-                                        (acc || part > 0 || t > 0) ? 1u : 0u);
+                    tc::mma_f16_ts_warp(to, tp + p_col(t, part == 1), vd + (uint64_t)(t * (2048 >> 4)),
+                                        (m64m >> x) & 1 ? id_o64 : id_o128, (acc || part > 0 || t > 0) ? 1u : 0u);
         };
         bool ok = true;
         int gj = 0, pc[kTiles] = {0, 0};
@@ -483,6 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(&bars[bItemEmpty + slot]);
             if (it.stop) break;
             const int ntiles = it.rows1 ? 2 : 1, nkv = max(it.nkv0, it.nkv1);
+            m64m = it.split ? (it.rows0 <= 64 ? 3 : 0) : (it.rows0 <= 64 ? 1 : 0) | (it.rows1 > 0 && it.rows1 <= 64 ? 2 : 0);
             ok = wait_warp(&bars[bQFull], k & 1, kWaitLimitCycles) &&
                  wait_warp(&bars[bKFull + (gj & 1)], (gj >> 1) & 1, kWaitLimitCycles);
             if (!ok) break;
@@ -592,7 +597,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int pos0_x = split ? it.pos00 : it.pos00 + x * it.rstep;
             const int nkv_x = split ? (nkv - x + 1) / 2 : (x ? it.nkv1 : it.nkv0);
             const int kstep = split ? 2 : 1, kfirst = split ? x : 0;
-            const int my_pos = r < rows_x ? pos0_x + r : pos0_x + rows_x - 1;   // last key this row sees
+            // the tile row this thread holds: lane 32 q + i holds row 32 q + i (M = 128) or, for a
+            // tile of 64 rows or fewer (M = 64 products), row 16 q + i for i < 16 and none above
+            const bool m64 = rows_x <= 64;
+            const int rr = m64 ? (lane < 16 ? 16 * (warp % 4) + lane : kRows) : r;
+            const int my_pos = rr < rows_x ? pos0_x + rr : pos0_x + rows_x - 1;   // last key this row sees
             float m_run = -INFINITY, l_run = 0.f;
             // the slot that zeroes V rows past the context (before its product reads them)
             const bool zero_duty = split ? x == ((nkv - 1) & 1) : (x == 0) == (it.nkv0 == nkv);
@@ -780,7 +789,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int qq = 0; qq < 8; qq++) {
                     const int lr = 4 * qq + (lane >> 3), unit = lane & 7;
                     const uint4 w = *reinterpret_cast<const uint4 *>(wb + lr * 128 + ((unit ^ (lr & 7)) << 4));
-                    const int trow = wrow0 + lr;
+                    const int trow = m64 ? (lr < 16 ? 16 * (warp % 4) + lr : kRows) : wrow0 + lr;
                     if (trow < rows_x) *reinterpret_cast<uint4 *>(obase + (size_t)trow * rstride + 64 * p + 8 * unit) = w;
                 }
                 __syncwarp();
