@@ -625,20 +625,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < 4; c++) tc::tmem_ld32(tS + 32 * c, sr[c]);
 #pragma unroll
                     for (int c = 0; c < 4; c++) tc::tmem_wait_ld(sr[c]);
-                    if (full) {
 #pragma unroll
-                        for (int c = 0; c < 4; c++)
+                    for (int c = 0; c < 4; c++) {
+                        if (!full) {
+                            // keys after the row's position: the score becomes -inf, in the registers
+                            // for the maximum and in TMEM for pass 2 (whose exponent then gives 0),
+                            // so that both passes run the same unmasked code on every tile
+                            const int t = lim - 32 * c;          // keys 0..t of this chunk are visible
 #pragma unroll
-                            for (int i = 0; i < 32; i += 2)
-                                mxs[(i >> 1) & 3] = max3(mxs[(i >> 1) & 3], __uint_as_float(sr[c][i]),
-                                                         __uint_as_float(sr[c][i + 1]));
-                    } else {
+                            for (int i = 0; i < 32; i++) sr[c][i] = i <= t ? sr[c][i] : 0xff800000u;
+                            tc::tmem_st32(tS + 32 * c, sr[c]);
+                        }
 #pragma unroll
-                        for (int c = 0; c < 4; c++)
-#pragma unroll
-                            for (int i = 0; i < 32; i++)
-                                if (32 * c + i <= lim) mxs[i & 3] = fmaxf(mxs[i & 3], __uint_as_float(sr[c][i]));
+                        for (int i = 0; i < 32; i += 2)
+                            mxs[(i >> 1) & 3] = max3(mxs[(i >> 1) & 3], __uint_as_float(sr[c][i]),
+                                                     __uint_as_float(sr[c][i + 1]));
                     }
+                    if (!full) tc::tmem_wait_st();
                 }
                 // pass 2 reads the scores again chunk by chunk, each load in flight while the
                 // previous chunk is computed; the first one already now
@@ -681,7 +684,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // pass 2, probabilities written over the scores
                 // exponents and row sums two lanes at a time (packed fp32 pairs)
-                const unsigned long long c2x2 = pack2(c2, c2), negm2 = pack2(-m_run, -m_run);
+                // (a row that sees no key yet has m_run = -inf and only -inf scores: its
+                // exponents are taken against 0, so that they give 0 and not NaN)
+                const float mref = m_run == -INFINITY ? 0.f : m_run;
+                const unsigned long long c2x2 = pack2(c2, c2), negm2 = pack2(-mref, -mref);
                 unsigned long long ls2[2] = {0ull, 0ull};
 #pragma unroll
                 for (int c = 0; c < 4; c++) {
@@ -694,12 +700,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 32; i += 2) {
                         const unsigned long long xx =
                             fma2(pack2(__uint_as_float(sc[i]), __uint_as_float(sc[i + 1])), c2x2, negm2);
-                        float p0 = fast_exp2(lo2(xx));
-                        float p1 = fast_exp2(hi2(xx));
-                        if (!full) {
-                            p0 = kc + i <= lim ? p0 : 0.f;
-                            p1 = kc + i + 1 <= lim ? p1 : 0.f;
-                        }
+                        const float p0 = fast_exp2(lo2(xx));
+                        const float p1 = fast_exp2(hi2(xx));
                         ls2[(i >> 1) & 1] = add2(ls2[(i >> 1) & 1], pack2(p0, p1));
                         const uint32_t hi = pack16<T>(p0, p1);
                         pk[i / 2] = hi;
@@ -767,23 +769,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             T *obase = reinterpret_cast<T *>(a.out) +
                        ((size_t)(it.q_begin + it.t0 + x * it.rstep) * a.num_heads + (x ? it.h1 : it.h)) * D;
             const size_t rstride = (size_t)a.num_heads * D;
+            // 32 output columns (unscaled) into the warp's buffer as 16-byte units
+            auto stage_chunk = [&](int c, const uint32_t (&o)[32]) {
 #pragma unroll
-            for (int p = 0; p < NP; p++) {
-#pragma unroll
-                for (int c = 0; c < 2; c++) {
-                    uint32_t o[32];
-                    load_out(64 * p + 32 * c, o);
-#pragma unroll
-                    for (int v = 0; v < 4; v++) {
-                        uint4 w;
-                        w.x = pack16<T>(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
-                        w.y = pack16<T>(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
-                        w.z = pack16<T>(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
-                        w.w = pack16<T>(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-                        const int unit = 4 * c + v;
-                        *reinterpret_cast<uint4 *>(wb + lane * 128 + ((unit ^ (lane & 7)) << 4)) = w;
-                    }
+                for (int v = 0; v < 4; v++) {
+                    uint4 w;
+                    w.x = pack16<T>(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
+                    w.y = pack16<T>(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
+                    w.z = pack16<T>(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
+                    w.w = pack16<T>(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
+                    const int unit = 4 * c + v;
+                    *reinterpret_cast<uint4 *>(wb + lane * 128 + ((unit ^ (lane & 7)) << 4)) = w;
                 }
+            };
+            // the buffer's 32 rows of panel p to global memory, 4 whole 128-byte row segments per store
+            auto store_panel = [&](int p) {
                 __syncwarp();
 #pragma unroll
                 for (int qq = 0; qq < 8; qq++) {
@@ -793,6 +793,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (trow < rows_x) *reinterpret_cast<uint4 *>(obase + (size_t)trow * rstride + 64 * p + 8 * unit) = w;
                 }
                 __syncwarp();
+            };
+            if (!split) {
+                // each chunk's TMEM load is in flight while the previous chunk is staged and stored
+                uint32_t ob[2][32];
+                tc::tmem_ld32(tO, ob[0]);
+#pragma unroll
+                for (int q = 0; q < D / 32; q++) {
+                    tc::tmem_wait_ld(ob[q & 1]);
+                    if (q + 1 < D / 32) tc::tmem_ld32(tO + 32 * (q + 1), ob[(q + 1) & 1]);
+                    stage_chunk(q & 1, ob[q & 1]);
+                    if (q & 1) store_panel(q >> 1);
+                }
+            } else {
+#pragma unroll
+                for (int p = 0; p < NP; p++) {
+#pragma unroll
+                    for (int c = 0; c < 2; c++) {
+                        uint32_t o[32];
+                        load_out(64 * p + 32 * c, o);
+                        stage_chunk(c, o);
+                    }
+                    store_panel(p);
+                }
             }
             if (split) {
                 // the other slot's O has been read: its softmax threads may go on
