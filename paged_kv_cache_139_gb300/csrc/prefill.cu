@@ -689,11 +689,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float mref = m_run == -INFINITY ? 0.f : m_run;
                 const unsigned long long c2x2 = pack2(c2, c2), negm2 = pack2(-mref, -mref);
                 unsigned long long ls2[2] = {0ull, 0ull};
+                // (for bf16, whose probabilities take twice the instructions, a loop over pairs of
+                // chunks, not unrolled: the kernel's code stays small)
+                constexpr int kPairUnroll = kBf16 ? 1 : 2;
+#pragma unroll kPairUnroll
+                for (int cc = 0; cc < 4; cc += 2)
 #pragma unroll
-                for (int c = 0; c < 4; c++) {
-                    uint32_t (&sc)[32] = sb[c & 1];
+                for (int h = 0; h < 2; h++) {
+                    const int c = cc + h;
+                    uint32_t (&sc)[32] = sb[h];
                     tc::tmem_wait_ld(sc);
-                    if (c < 3) tc::tmem_ld32(tS + 32 * (c + 1), sb[(c + 1) & 1]);
+                    if (c < 3) tc::tmem_ld32(tS + 32 * (c + 1), sb[h ^ 1]);
                     const int kc = 32 * c;
                     uint32_t pk[kBf16 ? 32 : 16];
 #pragma unroll
