@@ -627,11 +627,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < 4; c++) tc::tmem_wait_ld(sr[c]);
 #pragma unroll
                     for (int c = 0; c < 4; c++) {
-                        if (!full) {
+                        // keys 0..t of this chunk are visible to this row
+                        const int t = lim - 32 * c;
+                        if (!full && __any_sync(0xffffffffu, t < 31)) {
                             // keys after the row's position: the score becomes -inf, in the registers
                             // for the maximum and in TMEM for pass 2 (whose exponent then gives 0),
                             // so that both passes run the same unmasked code on every tile
-                            const int t = lim - 32 * c;          // keys 0..t of this chunk are visible
 #pragma unroll
                             for (int i = 0; i < 32; i++) sr[c][i] = i <= t ? sr[c][i] : 0xff800000u;
                             tc::tmem_st32(tS + 32 * c, sr[c]);
@@ -656,7 +657,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_run = m_new;
                 // O of the previous tiles is complete (its products were issued before this S)
                 if (i > 0 && __any_sync(0xffffffffu, moved)) {
-#pragma unroll
+                    // (rare after a row's first tiles: a loop, not unrolled, keeps the code small)
+#pragma unroll 1
                     for (int c = 0; c < D / 32; c++) {
                         uint32_t o[32];
                         tc::tmem_ld32(tO + 32 * c, o);
@@ -812,7 +814,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (q & 1) store_panel(q >> 1);
                 }
             } else {
-#pragma unroll
+#pragma unroll 1
                 for (int p = 0; p < NP; p++) {
 #pragma unroll
                     for (int c = 0; c < 2; c++) {
