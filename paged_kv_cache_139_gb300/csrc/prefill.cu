@@ -34,8 +34,10 @@
 //     gives its key tiles alternately to both tiles' TMEM and softmax warps
 //     (each pair of key tiles then overlaps as the two tiles of a pair do),
 //     and the two partial outputs are merged at the end.
-//   * Four softmax warps per tile (one thread per row) read S from TMEM, mask
-//     keys after the row's position, keep a running max and sum in fp32 (log2
+//   * Four softmax warps per tile (one thread per row) read S from TMEM (on a
+//     tile that crosses the diagonal they first overwrite the scores of keys
+//     after the row's position with -inf, so that every tile runs the same
+//     unmasked code), keep a running max and sum in fp32 (log2
 //     domain; the reference max moves only when it grows by more than 8, so
 //     probabilities stay below 2^8), write P as 16-bit over the scores in
 //     TMEM (for bf16 as a rounded part and its remainder) and rescale O in
