@@ -165,6 +165,51 @@ template <> __device__ __forceinline__ uint32_t pack16<__nv_bfloat16>(float x, f
 // fp16 (11 bits) needs one.
 __device__ __forceinline__ uint32_t p_col(int t, bool lo) { return 32 * (t >> 1) + 8 * (t & 1) + (lo ? 16 : 0); }
 
+// A tile's products as one run of one elected lane (one election, the operands'
+// descriptors stepped by immediates).  The offsets follow the shared-memory and
+// TMEM layouts above: S = Q K^T steps 32 bytes along a 64-element panel (2 in
+// descriptor units) and a panel (kPanelBytes >> 4 = 1024) after four steps;
+// O += P V steps the P columns as p_col and V by 16 keys (2048 bytes, 128 units).
+#define PKV_SS(o, acc) "add.s64 qa, %1, " #o ";\n\tadd.s64 kb, %2, " #o ";\n\t" \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [%0], qa, kb, %3, " acc ";\n\t"
+#define PKV_TS(ao, bo, acc) "add.u32 ta, %1, " #ao ";\n\tadd.s64 vb, %2, " #bo ";\n\t" \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], vb, %3, " acc ";\n\t"
+#define PKV_RUN_HEAD "{\n\t.reg .pred e, t, f, pa;\n\t.reg .b64 qa, kb, vb;\n\t.reg .b32 ta;\n\t" \
+    "setp.ne.b32 f, %4, %4;\n\tsetp.eq.b32 t, %4, %4;\n\tsetp.ne.b32 pa, %5, 0;\n\t" \
+    "elect.sync _|e, 0xffffffff;\n\t"
+
+// S = Q K^T over the head dimension (the first product overwrites).
+template <int D> __device__ __forceinline__ void mma_s_run(uint32_t d, uint64_t qd, uint64_t kd, uint32_t idesc) {
+    if constexpr (D == 128) {
+        asm volatile(PKV_RUN_HEAD PKV_SS(0, "f") PKV_SS(2, "t") PKV_SS(4, "t") PKV_SS(6, "t")
+                     PKV_SS(1024, "t") PKV_SS(1026, "t") PKV_SS(1028, "t") PKV_SS(1030, "t") "}"
+                     ::"r"(d), "l"(qd), "l"(kd), "r"(idesc), "r"(0u), "r"(0u) : "memory");
+    } else {
+        asm volatile(PKV_RUN_HEAD PKV_SS(0, "f") PKV_SS(2, "t") PKV_SS(4, "t") PKV_SS(6, "t") "}"
+                     ::"r"(d), "l"(qd), "l"(kd), "r"(idesc), "r"(0u), "r"(0u) : "memory");
+    }
+}
+
+// O (+)= P V over the tile's 128 keys, P from TMEM (a = its first column), the first product
+// accumulating when `acc`; for bf16 also the remainder part (columns + 16).
+template <bool kLo> __device__ __forceinline__ void mma_o_run(uint32_t d, uint32_t a, uint64_t vd, uint32_t idesc,
+                                                            uint32_t acc) {
+    if constexpr (!kLo) {
+        asm volatile(PKV_RUN_HEAD PKV_TS(0, 0, "pa") PKV_TS(8, 128, "t") PKV_TS(32, 256, "t") PKV_TS(40, 384, "t")
+                     PKV_TS(64, 512, "t") PKV_TS(72, 640, "t") PKV_TS(96, 768, "t") PKV_TS(104, 896, "t") "}"
+                     ::"r"(d), "r"(a), "l"(vd), "r"(idesc), "r"(0u), "r"(acc) : "memory");
+    } else {
+        asm volatile(PKV_RUN_HEAD PKV_TS(0, 0, "pa") PKV_TS(8, 128, "t") PKV_TS(32, 256, "t") PKV_TS(40, 384, "t")
+                     PKV_TS(64, 512, "t") PKV_TS(72, 640, "t") PKV_TS(96, 768, "t") PKV_TS(104, 896, "t")
+                     PKV_TS(16, 0, "t") PKV_TS(24, 128, "t") PKV_TS(48, 256, "t") PKV_TS(56, 384, "t")
+                     PKV_TS(80, 512, "t") PKV_TS(88, 640, "t") PKV_TS(112, 768, "t") PKV_TS(120, 896, "t") "}"
+                     ::"r"(d), "r"(a), "l"(vd), "r"(idesc), "r"(0u), "r"(acc) : "memory");
+    }
+}
+#undef PKV_SS
+#undef PKV_TS
+#undef PKV_RUN_HEAD
+
 // Ticket t in [0, num_items): the tiles with the most keys first (row-tile or
 // pair index descending), then sequence, then head (or head pair: h is its
 // first head).
@@ -459,23 +504,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto issue_s = [&](int x, int stg, int qx) {
             const uint64_t kd = k_desc + (uint64_t)(stg * kStageStep);
             const uint64_t qd = q_desc + (uint64_t)(qx * kStageStep);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; kk++) {
-                const uint32_t off = ((kk / 4) * kPanelBytes + (kk % 4) * 32) >> 4;
-                tc::mma_f16_ss_warp(tmem + x * kTileCols, qd + off, kd + off, (m64m >> x) & 1 ? id_s64 : id_s128,
-                                    kk > 0);
-            }
+            mma_s_run<D>(tmem + x * kTileCols, qd, kd, (m64m >> x) & 1 ? id_s64 : id_s128);
             tc::mma_commit_warp(&bars[bSFull + x]);
         };
         auto issue_o = [&](int x, int stg, bool acc) {
             const uint64_t vd = v_desc + (uint64_t)(stg * kStageStep);
             const uint32_t tp = tmem + x * kTileCols, to = tp + kKeys;
-#pragma unroll
-            for (int part = 0; part < (kBf16 ? 2 : 1); part++)
-#pragma unroll
-                for (int t = 0; t < kKeys / 16; t++)
-                    tc::mma_f16_ts_warp(to, tp + p_col(t, part == 1), vd + (uint64_t)(t * (2048 >> 4)),
-                                        (m64m >> x) & 1 ? id_o64 : id_o128, (acc || part > 0 || t > 0) ? 1u : 0u);
+            mma_o_run<kBf16>(to, tp, vd, (m64m >> x) & 1 ? id_o64 : id_o128, acc ? 1u : 0u);
         };
         bool ok = true;
         int gj = 0, pc[kTiles] = {0, 0};
