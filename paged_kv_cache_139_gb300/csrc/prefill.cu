@@ -486,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // item's first O product (which overwrites O) waits for that tile's first P, which its
         // softmax threads write only after they have read this item's O.
         // The whole warp runs the loop (its waits and descriptors are warp-uniform values); one
-        // elected lane issues each product and commit.
+        // elected lane issues each tile's run of products (one election per run) and each commit.
         // A tile of 64 rows or fewer takes M = 64 products (half the tensor work); their rows
         // sit in TMEM lanes 0-15 of each 32-lane quarter (row r in lane 32 (r / 16) + r % 16).
         const uint32_t id_s128 = tc::idesc_f16(kRows, kKeys, kBf16, false), id_s64 = tc::idesc_f16(64, kKeys, kBf16, false);

@@ -94,7 +94,7 @@ const char *pkv_last_error_string(void) { return pkv::t_msg; }
 
 uint64_t pkv_launch_count(void) { return pkv::g_launches.load(std::memory_order_relaxed); }
 
-int pkv_version(void) { return 113; }
+int pkv_version(void) { return 114; }
 
 pkv_status pkv_check(struct CUstream_st *stream) {
     cudaError_t e = cudaStreamSynchronize(stream);
