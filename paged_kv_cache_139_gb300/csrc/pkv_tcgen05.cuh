@@ -67,54 +67,11 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool bf16, bool b
 
 // ---- MMA issue and completion ------------------------------------------------
 
-// One thread: D[tmem] (+)= A[smem desc] * B[smem desc]^T for the shape and
-// types in idesc; accumulate != 0 adds to D, 0 overwrites it.
-__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                           uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Same with A read from TMEM (M rows in lanes, 16-bit elements packed two
-// per column, the lower half holding the even K index).
-__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
-                                           uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Whole warp, converged, every lane passing the same operands: one elected
-// lane issues the MMA (so the operands stay warp-uniform values and the
-// issuing code is not a divergent branch).  Otherwise as mma_f16_ss / _ts.
-__device__ __forceinline__ void mma_f16_ss_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                                uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_f16_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
-                                                uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
+// The products themselves are issued where their operand layouts are known
+// (a run of one elected lane per tile in the prompt-phase kernel): the
+// instruction is tcgen05.mma.cta_group::1.kind::f16 [D], A, B, idesc, acc with
+// A and B shared-memory descriptors (or A a TMEM address), acc a predicate
+// (false: D is overwritten).
 
 // Whole warp, converged: one elected lane commits (see mma_commit).
 __device__ __forceinline__ void mma_commit_warp(uint64_t *bar) {
