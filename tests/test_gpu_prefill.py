@@ -262,14 +262,16 @@ def test_unprepared_workspace_is_refused(cuda_device):
     assert torch.equal(c.rerun(), c.out)
 
 
-@pytest.mark.parametrize("dtype,H,Hkv", [("f16", 4, 4), ("bf16", 8, 2)])
+@pytest.mark.parametrize("dtype,H,Hkv", [("f16", 4, 4), ("bf16", 8, 2), ("bf16", 6, 2), ("bf16", 3, 3)])
 def test_one_tile_items_split_over_both_groups(cuda_device, dtype, H, Hkv):
     """Items with one query tile and two or more key tiles give their key tiles
     alternately to both softmax groups and merge the two outputs.  The
     contexts cover 2 to 8 key tiles, a last key tile ending mid-tile on
     either group (its rows past the context zeroed by that group), rows that
-    see no key of the second group's first tile (positions below 128), and
-    the one-tile remainder after a pair of tiles."""
+    see no key of the second group's first tile (positions below 128: their
+    scores there are all -inf), and the one-tile remainder after a pair of
+    tiles.  An even number of query heads per kv head pairs heads instead
+    (no one-tile items), so bf16 is also run with groups of 3 and 1."""
     ctx = (200, 259, 484, 1000, 130, 900)
     new = (128, 5, 50, 1, 2, 300)
     _check(PrefillCase(custom(ctx, new, H=H, Hkv=Hkv, dtype=dtype), cuda_device), f"split items {dtype}")
