@@ -163,7 +163,11 @@ template <> __device__ __forceinline__ uint32_t pack16<__nv_bfloat16>(float x, f
 // would see their rounding in its output, so for bf16 P = P_hi + P_lo (both
 // bf16, together 16 significant bits) and both products are accumulated;
 // fp16 (11 bits) needs one.
-__device__ __forceinline__ uint32_t p_col(int t, bool lo) { return 32 * (t >> 1) + 8 * (t & 1) + (lo ? 16 : 0); }
+constexpr uint32_t p_col(int t, bool lo) { return 32 * (t >> 1) + 8 * (t & 1) + (lo ? 16 : 0); }
+// (the product runs below write these columns as immediates)
+static_assert(p_col(1, false) == 8 && p_col(2, false) == 32 && p_col(3, false) == 40 && p_col(7, false) == 104 &&
+                  p_col(0, true) == 16 && p_col(5, true) == 88 && p_col(7, true) == 120,
+              "P column layout");
 
 // A tile's products as one run of one elected lane (one election, the operands'
 // descriptors stepped by immediates).  The offsets follow the shared-memory and
