@@ -174,6 +174,8 @@ static_assert(p_col(1, false) == 8 && p_col(2, false) == 32 && p_col(3, false) =
 // TMEM layouts above: S = Q K^T steps 32 bytes along a 64-element panel (2 in
 // descriptor units) and a panel (kPanelBytes >> 4 = 1024) after four steps;
 // O += P V steps the P columns as p_col and V by 16 keys (2048 bytes, 128 units).
+static_assert((kPanelBytes >> 4) == 1024 && (32 >> 4) == 2 && ((16 * 128) >> 4) == 128 && kKeys == 128,
+              "descriptor steps written as immediates in the product runs");
 #define PKV_SS(o, acc) "add.s64 qa, %1, " #o ";\n\tadd.s64 kb, %2, " #o ";\n\t" \
     "@e tcgen05.mma.cta_group::1.kind::f16 [%0], qa, kb, %3, " acc ";\n\t"
 #define PKV_TS(ao, bo, acc) "add.u32 ta, %1, " #ao ";\n\tadd.s64 vb, %2, " #bo ";\n\t" \
