@@ -45,3 +45,14 @@ def test_compact_sample_keeps_shared_blocks_once():
     for i in range(len(sel)):
         nb = -(-int(c2[i]) // w.block_size)
         assert int(sl2[i]) // w.block_size in set(t2[i][:nb].tolist())
+
+
+def test_profiles_carry_traffic_for_the_current_library():
+    """Every workload whose bench line reports roofline.traffic finds a DRAM
+    traffic line under profiles/ for the library version that is built, so a
+    version bump without new (or carried-over) ncu figures is caught here."""
+    import paged_kv_cache_139_gb300 as pkv
+    v = pkv.version()
+    for name in ("llama7b_B16_d128", "opt13b", "sampling", "longgqa", "prefix", "swap"):
+        t = bench.profile_traffic(name, v)
+        assert t is not None and t > 0, f"no traffic_bytes_per_launch[{name}@{v}] under profiles/"
